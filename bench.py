@@ -1,0 +1,469 @@
+"""Benchmark: restricted-vocabulary MTP draft head + greedy verify on GB300.
+
+One bench step = one MTP3 draft chain on the single-stream decode workload:
+three sequential draft-head calls (B = 1, a fresh hidden vector each) on a
+65,536-row x 2048 bf16 candidate head drawn from the 248,320-row output head.
+`value` is draft steps/s (3 calls per bench step) measured on the device with
+CUDA events around each call, with L2 flushed (256 MiB write) before every
+call and outside the timed events, so every call reads the 268 MB head from
+HBM.  The same run also measures (reported under "verify", "sweep" and
+"nvfp4"): the batched greedy verify (64 x 4 rows against the full head), the
+head-size sweep (248,320 / 65,536 / 32,768 rows) and the 4-bit head
+(65,536 x 4096, B = 1 and 8).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (the only reference implementation
+this method has) on the host cores, on the same workload and metric.
+Under torchrun each rank runs an independent replica on its own GPU
+(no data-path collective); value = all ranks' draft steps / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft steps/s and verify rounds/s; head HBM GB/s as % of GB300 roofline"
+UNIT = "draft steps/s"
+WORKLOAD = ("draft head: 65,536 sorted candidate rows of a 248,320 x 2048 bf16 head ~N(0,0.02) (seed 2), "
+            "B=1 hidden ~N(0,1), 3 sequential draft steps per bench step")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+
+        def pick(*names):
+            for n in names:
+                if n in d and isinstance(d[n], (int, float)):
+                    return float(d[n])
+            return None
+        hbm = pick("hbm_gbs", "hbm_GBps", "hbm")
+        bf = pick("bf16_tflops", "bf16_TFLOPs")
+        bfs = pick("bf16_tflops_sustained")
+        if hbm and bf:
+            return {"hbm_gbs": hbm, "bf16_tflops": bf, "bf16_tflops_sustained": bfs or bf}, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# device timing helpers
+
+class Timer:
+    """Per-call device time with CUDA events on the current stream; L2 is
+    flushed before each call, outside the events."""
+
+    def __init__(self, torch, flush=True):
+        self.torch = torch
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush else None
+
+    def flush(self):
+        if self.flush_buf is not None:
+            self.flush_buf.fill_(1)
+
+    def time_calls(self, fn, n, warmup=3):
+        torch = self.torch
+        for _ in range(warmup):
+            self.flush()
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            self.flush()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in evs]  # microseconds
+
+
+def stats(us):
+    us = sorted(us)
+    return {"median_us": round(statistics.median(us), 3), "p10_us": round(us[len(us) // 10], 3),
+            "p90_us": round(us[(len(us) * 9) // 10], 3), "mean_us": round(sum(us) / len(us), 3)}
+
+
+def profile_traffic(kernel_file: str, summary: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (sha256 of the .cu file); else None."""
+    try:
+        src = open(os.path.join(ROOT, "verify_head_gb300", "csrc", kernel_file), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        vals = {}
+        for line in open(os.path.join(ROOT, "profiles", summary)):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("source_sha256_16") == sha and "dram_bytes_per_launch" in vals:
+            return float(vals["dram_bytes_per_launch"])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def load_verify_golden():
+    """Draft ids (inputs) and the oracle's greedy ids for the batched-verify
+    workload, stored by tests/golden/make_verify_golden.py."""
+    path = os.path.join(ROOT, "tests", "golden", "verify_b64_k3_248320x2048.txt")
+    nid = np.zeros(256, np.int32)
+    draft = np.zeros((64, 3), np.int32)
+    for line in open(path):
+        p = line.split()
+        if p and p[0] == "row":
+            nid[int(p[1])] = int(p[2])
+        elif p and p[0] == "seq":
+            draft[int(p[1])] = [int(v) for v in p[2:5]]
+    return {"next_ids": nid, "draft": draft}
+
+
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import synth
+    import verify_head_gb300 as vh
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    vh.lib()
+    dev = torch.device("cuda")
+    peaks, peak_src = load_peaks()
+
+    def t_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # ---- headline workload: draft head 65,536 x 2048, B=1, 3 steps ----
+    case = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
+    W = t_bf16(case.W)
+    cand = torch.from_numpy(case.cand_ids).to(dev)
+    xs = [t_bf16(h) for h in case.hidden]
+    ws = vh.workspace(1)
+    ids = [torch.empty(1, dtype=torch.int32, device=dev) for _ in range(3)]
+    mls = [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(3)]
+    timer = Timer(torch)
+
+    def call(i):
+        vh.mtp_draft_head_argmax(xs[i], W, cand, ids=ids[i], maxlogit=mls[i], ws=ws)
+
+    bytes_per_call = case.Vc * case.H * 2 + case.Vc * 4 + case.B * case.H * 2
+
+    for _ in range(max(3, args.warmup)):
+        for i in range(3):
+            timer.flush()
+            call(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        per_call = []
+        evs = []
+        for _ in range(args.steps):
+            for i in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                timer.flush()
+                a.record()
+                call(i)
+                b.record()
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        per_call = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    total_s = sum(per_call) * 1e-6
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+        torch.distributed.barrier()
+    n_calls = 3 * args.steps
+    value = world * n_calls / total_s
+    st = stats(per_call)
+    avg_us = sum(per_call) / len(per_call)
+    achieved = bytes_per_call / (avg_us * 1e-6) / 1e9
+
+    # ---- end to end through the binding: pinned host hidden in, ids out ----
+    host_x = [torch.from_numpy(np.ascontiguousarray(h).view(np.int16)).pin_memory() for h in case.hidden]
+    host_ids = torch.empty(3, dtype=torch.int32).pin_memory()
+    host_ml = torch.empty(3, dtype=torch.float32).pin_memory()
+    dx = [torch.empty(1, 2048, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    e2e_us = []
+    e2e_steps = max(5, args.steps // 2)
+    for it in range(e2e_steps + 2):
+        timer.flush()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(3):
+            dx[i].view(torch.int16).copy_(host_x[i], non_blocking=True)
+            vh.mtp_draft_head_argmax(dx[i], W, cand, ids=ids[i], maxlogit=mls[i], ws=ws)
+            host_ids[i:i + 1].copy_(ids[i], non_blocking=True)
+            host_ml[i:i + 1].copy_(mls[i], non_blocking=True)
+        b.record()
+        b.synchronize()
+        if it >= 2:
+            e2e_us.append(a.elapsed_time(b) * 1e3)
+    e2e_value = world * 3 * len(e2e_us) / (sum(e2e_us) * 1e-6)
+    del W
+
+    extra = {}
+    if rank == 0 and not args.skip_extra:
+        extra = measure_extra(torch, vh, synth, timer, peaks, load_verify_golden)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cpu = cpu_baseline(case, seconds=args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(total_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generators; no corpus or trained weights)",
+        "config": {"workload": WORKLOAD, "Vc": case.Vc, "H": case.H, "B": case.B, "draft_steps_per_step": 3,
+                   "l2": "flushed before every call (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "draft_call": st,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+                     "frac_of_8000_spec": round(achieved / 8000.0, 4),
+                     "traffic": profile_traffic("gemv_argmax.cu", "draft_gemv_65536x2048.txt"),
+                     "algorithmic_bytes_per_launch": bytes_per_call,
+                     "kernel": "k_gemv_bf16<1> (split-V streaming GEMV + fused argmax)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": 3 * case.H * 2,
+                "d2h_bytes_per_step": 3 * 8, "median_us_per_step": round(statistics.median(e2e_us), 2)},
+        "gpu_launches": n_calls,
+        "clocks": sampler.summary(),
+        "cpu_baseline": cpu,
+    }
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
+    dev = torch.device("cuda")
+    out = {}
+
+    def t_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # ---- batched greedy verify: 64 x 4 rows vs 248,320 x 2048 ----
+    vc = synth.verify_case(B=64, k=3, H=2048, V=synth.V_FULL, seed_w=2, seed=4, with_head=True)
+    Wf = t_bf16(vc.W)
+    X = t_bf16(vc.X)
+    gold = load_verify_golden()
+    draft = torch.from_numpy(gold["draft"]).to(dev)
+    ws = vh.workspace(256)
+    acc = torch.empty(64, dtype=torch.int32, device=dev)
+    nid = torch.empty(256, dtype=torch.int32, device=dev)
+    ml = torch.empty(256, dtype=torch.float32, device=dev)
+    for path, name in ((vh.VH_PATH_TENSOR, "verify"), (vh.VH_PATH_CUDA_CORE, "verify_cuda_core")):
+        us = timer.time_calls(lambda: vh.spec_verify_greedy(X, Wf, draft, 64, 3, accept_len=acc, next_ids=nid,
+                                                            row_maxlogit=ml, ws=ws, path=path),
+                              5 if path == vh.VH_PATH_TENSOR else 2, warmup=2 if path == vh.VH_PATH_TENSOR else 1)
+        med = statistics.median(us)
+        nbytes = vc.W.nbytes + vc.X.nbytes
+        flops = 2.0 * 256 * synth.V_FULL * 2048
+        a = acc.cpu().numpy()
+        out[name] = {
+            "workload": "64 seqs x (k+1)=4 rows x 2048 bf16 vs full 248,320 x 2048 bf16 head (seeds 2/4), "
+                        "draft ids = oracle greedy ids corrupted w.p. 0.45",
+            "rounds_per_s": round(1e6 / med, 2), **stats(us),
+            "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+            "tflops": round(flops / (med * 1e-6) / 1e12, 1),
+            "tensor_frac_burst": round(flops / (med * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+            "accept_hist": np.bincount(a, minlength=4).tolist(), "mean_accept": round(float(a.mean()), 4),
+            "matches_stored_oracle_ids": int((nid.cpu().numpy() == gold["next_ids"]).sum()),
+            "gpu_launches_per_round": 1 if path == vh.VH_PATH_TENSOR else 32,
+        }
+    del Wf, X
+
+    # ---- head-size sweep, B=1 ----
+    sweep = {}
+    for Vc in (248_320, 65_536, 32_768):
+        c = synth.draft_case(Vc=Vc, H=2048, B=1, steps=1, seed=2, cand_seed=3)
+        Wc = t_bf16(c.W)
+        cc = torch.from_numpy(c.cand_ids).to(dev)
+        x = t_bf16(c.hidden[0])
+        w1 = vh.workspace(1)
+        us = timer.time_calls(lambda: vh.mtp_draft_head_argmax(x, Wc, cc, ws=w1), 20)
+        med = statistics.median(us)
+        nbytes = Vc * 2048 * 2 + Vc * 4 + 4096
+        sweep[str(Vc)] = {"steps_per_s": round(1e6 / med, 1), **stats(us),
+                          "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+                          "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+        del Wc
+    out["sweep"] = sweep
+
+    # ---- block-scaled 4-bit head 65,536 x 4096, B = 1 and 8 ----
+    nv = {}
+    for B in (1, 8):
+        c = synth.nvfp4_case(Vc=65_536, H=4096, B=B, steps=1, seed=5)
+        q = torch.from_numpy(c.q).to(dev)
+        s = torch.from_numpy(c.s).to(dev)
+        cc = torch.from_numpy(c.cand_ids).to(dev)
+        x = t_bf16(c.hidden[0])
+        wsb = vh.workspace(B)
+        us = timer.time_calls(lambda: vh.mtp_draft_head_argmax_nvfp4(x, q, s, c.g, cc, ws=wsb), 20)
+        med = statistics.median(us)
+        nbytes = c.q.nbytes + c.s.nbytes + 65_536 * 4 + B * 4096 * 2
+        nv[f"B{B}"] = {"steps_per_s": round(1e6 / med, 1), **stats(us),
+                       "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+                       "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    out["nvfp4"] = nv
+    return out
+
+
+def cpu_baseline(case, seconds: float = 10.0):
+    """The oracle, as it stands, on the host cores: whole draft steps of the
+    same workload until about `seconds` of CPU time have passed."""
+    import oracle
+    oracle.build()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.draft_argmax(case.hidden[n % 3], case.W, case.cand_ids)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The CPU oracle timed on this workload (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    oracle.build()
+    case = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
+    for _ in range(max(1, min(args.warmup, 2))):
+        oracle.draft_argmax(case.hidden[0], case.W, case.cand_ids)
+    per_step = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for i in range(3):
+            oracle.draft_argmax(case.hidden[i], case.W, case.cand_ids)
+        per_step.append(time.perf_counter() - t0)
+    total = sum(per_step)
+    value = 3 * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "Vc": case.Vc, "H": case.H, "B": case.B},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{args.steps} bench steps x 3 whole draft steps"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        args.steps = max(1, min(args.steps, 50))  # bounded: ~0.1-0.5 s of CPU per draft step
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * verifyhead — restricted-vocabulary MTP draft head and greedy speculative
+ * verification on one GPU (GB300, sm_103a).  C ABI of libverifyhead.so.
+ *
+ * Source of the method: "少读一张大表，草稿路径才真正快起来" in the Qwen3.8
+ * Flash dual-Spark tuning log (cnblogs): the MTP draft path scores a smaller
+ * candidate table (65,536 rows) instead of the 248,320-row full output head,
+ * takes the argmax and maps it to the global token id; the target model keeps
+ * the full head and verifies the draft.  "长上下文推理优化" §5 gives the
+ * speculative loop (MTP proposal -> target verification -> accept several
+ * tokens; acceptance rate and mean accepted tokens per step).  "为什么生产推理我
+ * 默认 vLLM" §3 names the NVFP4 4-bit weight format used for the 4-bit head.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must be device memory (or managed
+ *    memory) owned by the caller; the library never allocates, frees or
+ *    synchronises.  Work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and outputs are valid in stream order.
+ *  - Arguments are checked on the host before anything is launched; a failed
+ *    check returns a negative status and launches nothing.  VH_ERR_LAUNCH
+ *    reports a CUDA launch error (the workspace must then be re-zeroed).
+ *  - Argmax rule: the largest fp32 score wins; equal scores go to the lowest
+ *    global token id.  NaN scores count as -inf; -0 equals +0.
+ *  - bf16 tensors are passed as raw 16-bit patterns, row-major.
+ *  - Workspace: `ws` is a caller-owned device buffer of at least
+ *    vh_workspace_bytes(rows) bytes, 16-byte aligned, zeroed ONCE by the
+ *    caller after allocation.  Every call leaves it zeroed again, so
+ *    consecutive calls in one stream (or a captured CUDA graph) can reuse it
+ *    with no memset.  Calls that may overlap in time (different streams)
+ *    need different workspaces.
+ *  - No global state: calls are thread-safe given distinct workspaces.
+ */
+#ifndef VERIFYHEAD_H
+#define VERIFYHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VH_API __attribute__((visibility("default")))
+#else
+#define VH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VH_OK = 0,
+    VH_ERR_NULL = -1,      /* a required pointer is NULL */
+    VH_ERR_SHAPE = -2,     /* a size is out of range or not a required multiple */
+    VH_ERR_ALIGN = -3,     /* a pointer is not aligned as documented */
+    VH_ERR_WORKSPACE = -4, /* ws_bytes < vh_workspace_bytes(rows) */
+    VH_ERR_LAUNCH = -5,    /* CUDA reported an error when launching */
+    VH_ERR_DEVICE = -6     /* no usable CUDA device / unsupported architecture */
+} vh_status;
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+VH_API int vh_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+VH_API const char* vh_status_string(int status);
+
+/* Bytes of workspace needed by calls that produce `rows` argmax rows
+ * (rows = B for the draft heads, B*(k+1) for verification).  0 if rows < 1. */
+VH_API size_t vh_workspace_bytes(int rows);
+
+/*
+ * Restricted-vocabulary draft head, bf16 weights.
+ *
+ * For each hidden row b < B:
+ *     s[b,c]      = sum_h hidden[b,h] * W_cand[c,h]      (fp32 accumulation)
+ *     ids[b]      = cand_ids[argmax_c s[b,c]]            (lowest id on ties)
+ *     maxlogit[b] = max_c s[b,c]
+ * Scores are never written to memory.  ("少读一张大表": only the small
+ * candidate table is read; the winner is returned as a global token id.)
+ *
+ *  hidden    device, bf16 [B][H], 16-byte aligned
+ *  W_cand    device, bf16 [Vc][H] row-major, 32-byte aligned (a separate copy
+ *            of the candidate rows, not a view of the full head)
+ *  cand_ids  device, int32 [Vc], ascending and distinct (precondition, not
+ *            checked; ties are broken by id either way), values in [0, 2^31)
+ *  B         1 <= B <= 256 (processed in groups of 8 hidden rows; each group
+ *            reads W_cand once)
+ *  H         16 <= H <= 65536, H % 16 == 0
+ *  Vc        1 <= Vc <= 2^31 - 1
+ *  ids       device, int32 [B] (out)
+ *  maxlogit  device, fp32 [B] (out)
+ *  ws        device workspace, ws_bytes >= vh_workspace_bytes(B)
+ */
+VH_API vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const int32_t* cand_ids, int B, int H,
+                                int Vc, int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Restricted-vocabulary draft head, block-scaled 4-bit weights (NVFP4).
+ *
+ * Weight (c, h) = e2m1(code) * e4m3(scales[c][h/16]) * tensor_scale, where
+ * code is the low nibble of Wq[c][h/2] for even h and the high nibble for
+ * odd h; E2M1 = sign, 2 exponent bits (bias 1), 1 mantissa bit (magnitudes
+ * 0 0.5 1 1.5 2 3 4 6); E4M3 = OCP FP8 e4m3fn (bias 7, max 448).  Scores,
+ * ids and maxlogit are as for mtp_draft_head_argmax.  The tensor scale is
+ * applied after accumulation (the result equals the per-weight rule up to
+ * fp32 rounding).
+ *
+ *  hidden        device, bf16 [B][H], 16-byte aligned
+ *  Wq            device, uint8 [Vc][H/2], 32-byte aligned
+ *  scales        device, uint8 [Vc][H/16], 16-byte aligned
+ *  tensor_scale  finite, > 0
+ *  cand_ids      as above
+ *  B             1 <= B <= 256;  H: 64 <= H <= 65536, H % 64 == 0
+ *  ids, maxlogit, ws: as above
+ */
+VH_API vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                      float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
+                                      int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Greedy speculative verification over the full output head.
+ *
+ * Row r = b*(k+1) + j of `hidden` is the target model's hidden state for
+ * sequence b after its context plus draft tokens 0..j-1 (j = 0 is the
+ * position right after the last verified token).  Then
+ *     next_ids[r]     = argmax_v sum_h hidden[r,h] * W_full[v,h]   (lowest v on ties)
+ *     row_maxlogit[r] = the maximum score                          (optional)
+ *     accept_len[b]   = number of leading j < k with next_ids[b*(k+1)+j] == draft_ids[b*k+j]
+ * so sequence b emits draft_ids[b, 0..a-1] followed by next_ids[b*(k+1)+a]
+ * (the correction token, or the bonus token when a == k).
+ *
+ *  hidden        device, bf16 [B*(k+1)][H], 16-byte aligned
+ *  W_full        device, bf16 [V][H] row-major, 32-byte aligned
+ *  draft_ids     device, int32 [B][k]
+ *  B, k          B >= 1, 1 <= k <= 15, B*(k+1) <= 65536
+ *  H             16 <= H <= 65536, H % 16 == 0
+ *  V             1 <= V < 2^31
+ *  accept_len    device, int32 [B] (out), values in 0..k
+ *  next_ids      device, int32 [B*(k+1)] (out)
+ *  row_maxlogit  device, fp32 [B*(k+1)] (out) or NULL
+ *  ws            device workspace, ws_bytes >= vh_workspace_bytes(B*(k+1))
+ *
+ * Rows are processed in groups of at most 256 on the tensor cores (H % 64
+ * == 0) or 8 on CUDA cores (few rows, or other H); each group reads W_full
+ * once.
+ */
+VH_API vh_status spec_verify_greedy(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k, int H,
+                             int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Kernel selection for spec_verify_greedy_path. */
+typedef enum {
+    VH_PATH_AUTO = 0,      /* tensor cores when B*(k+1) > 8 and H % 64 == 0, else CUDA cores */
+    VH_PATH_CUDA_CORE = 1, /* streaming GEMV, groups of 8 rows */
+    VH_PATH_TENSOR = 2     /* tcgen05 skinny GEMM, groups of 256 rows; VH_ERR_SHAPE if H % 64 != 0 */
+} vh_path;
+
+/* spec_verify_greedy with an explicit kernel choice (same results up to fp32
+ * summation order). */
+VH_API vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k,
+                                  int H, int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit,
+                                  void* ws, size_t ws_bytes, void* stream, int path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFYHEAD_H */

@@ -1,0 +1,438 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI."""
+import os
+
+import numpy as np
+import pytest
+
+from parity_util import (TOL_4BIT, TOL_BF16, accept_scan, check_accept, check_ids, to_torch, to_torch_bf16)
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def vh():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import verify_head_gb300 as vh
+    vh.build()
+    vh.lib()
+    return vh
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+@pytest.fixture(scope="module")
+def syn():
+    import synth
+    synth.build()
+    return synth
+
+
+def run_draft(vh, x_bits, W_bits, cand, ws=None):
+    import torch
+    ids, ml = vh.mtp_draft_head_argmax(to_torch_bf16(x_bits), to_torch_bf16(W_bits), to_torch(cand), ws=ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), ml.cpu().numpy()
+
+
+def draft_score_of(orc, x_bits, W_bits, cand):
+    def f(r, gid):
+        c = int(np.searchsorted(cand, gid))
+        assert cand[c] == gid, "GPU returned an id outside the candidate set"
+        return orc.dot_bf16(x_bits[r], W_bits[c])
+    return f
+
+
+def check_draft(vh, orc, x, W, cand):
+    g_ids, g_ml = run_draft(vh, x, W, cand)
+    o_ids, o_ml, o_sec = orc.draft_argmax(x, W, cand)
+    check_ids(g_ids, g_ml, o_ids, o_ml, o_sec, draft_score_of(orc, x, W, cand), TOL_BF16)
+    return g_ids, g_ml
+
+
+# ----------------------------------------------------------------------------
+# bf16 draft head
+
+
+def test_tiny_workload(vh, orc, syn):
+    draft, verify, W_full = syn.tiny_case()
+    for x in draft.hidden:  # 3 sequential draft steps
+        check_draft(vh, orc, x, draft.W, draft.cand_ids)
+
+
+@pytest.mark.parametrize("Vc,H,B", [(1, 16, 1), (7, 64, 1), (1023, 256, 1), (1024, 256, 2), (1025, 272, 3),
+                                    (5000, 2048, 1), (3001, 2080, 5), (2500, 4096, 8), (700, 6144, 9),
+                                    (4099, 128, 17)])
+def test_draft_shapes(vh, orc, syn, Vc, H, B):
+    cand = syn.sorted_subset(Vc + H, 2, 300_000, Vc)
+    W = syn.normal_bf16(Vc + 7, 1, (Vc, H), 0.02)
+    x = syn.normal_bf16(B + 11, 3, (B, H), 1.0)
+    check_draft(vh, orc, x, W, cand)
+
+
+def test_draft_full_size_65536x2048(vh, orc, syn):
+    """The single-stream decode workload: 65,536 candidates x 2048, B=1, 3 steps."""
+    case = syn.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
+    for x in case.hidden:
+        check_draft(vh, orc, x, case.W, case.cand_ids)
+
+
+@pytest.mark.parametrize("Vc", [248_320, 65_536, 32_768])
+def test_head_size_sweep(vh, orc, syn, Vc):
+    case = syn.draft_case(Vc=Vc, H=2048, B=1, steps=1, seed=2, cand_seed=3)
+    check_draft(vh, orc, case.hidden[0], case.W, case.cand_ids)
+
+
+def test_zero_head_ties_to_lowest_id(vh, orc):
+    W = np.zeros((3000, 64), np.uint16)
+    cand = (np.arange(3000, dtype=np.int32) * 3 + 5)
+    x = np.full((2, 64), 0x3F80, np.uint16)
+    g_ids, g_ml = run_draft(vh, x, W, cand)
+    assert list(g_ids) == [5, 5] and list(g_ml) == [0.0, 0.0]
+
+
+def test_duplicate_rows_tie_to_lowest_id(vh, syn):
+    W = syn.normal_bf16(3, 1, (4096, 128), 0.02)
+    x = syn.normal_bf16(3, 3, (1, 128), 1.0)
+    xf = (x[0].astype(np.uint32) << 16).view(np.float32)
+    best = np.where(xf > 0, 0x3F00, 0xBF00).astype(np.uint16)  # +-0.5: the clear winner
+    for r in (100, 2000, 4000):  # same row three times, in different CTAs
+        W[r] = best
+    cand = np.arange(4096, dtype=np.int32)
+    g_ids, _ = run_draft(vh, x, W, cand)
+    assert g_ids[0] == 100
+
+
+def test_single_candidate(vh, syn):
+    W = syn.normal_bf16(4, 1, (1, 256), 0.02)
+    x = syn.normal_bf16(4, 3, (4, 256), 1.0)
+    g_ids, _ = run_draft(vh, x, W, np.array([123456], np.int32))
+    assert list(g_ids) == [123456] * 4
+
+
+def test_workspace_reused_and_left_zero(vh, syn):
+    import torch
+    case = syn.draft_case(Vc=20_000, H=512, B=3, steps=2, seed=9)
+    ws = vh.workspace(3)
+    Wd, cd = to_torch_bf16(case.W), to_torch(case.cand_ids)
+    outs = []
+    for x in case.hidden + case.hidden:
+        ids, ml = vh.mtp_draft_head_argmax(to_torch_bf16(x), Wd, cd, ws=ws)
+        outs.append((ids.cpu().numpy(), ml.cpu().numpy()))
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    for a, b in zip(outs[:2], outs[2:]):  # deterministic: same inputs, same bits
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_restricted_equals_full_when_top1_is_candidate(vh, syn):
+    """Invariant on the GPU: with W_cand = W_full[cand], the restricted argmax
+    equals the full argmax whenever the full top-1 is a candidate."""
+    V, H = 50_000, 512
+    W_full = syn.normal_bf16(21, 1, (V, H), 0.02)
+    all_ids = np.arange(V, dtype=np.int32)
+    cand = syn.sorted_subset(21, 2, V, 10_000)
+    for t in range(6):
+        x = syn.normal_bf16(40 + t, 3, (1, H), 1.0)
+        f_ids, f_ml = run_draft(vh, x, W_full, all_ids)
+        c = np.union1d(cand, f_ids).astype(np.int32) if t % 2 == 0 else cand
+        r_ids, r_ml = run_draft(vh, x, np.ascontiguousarray(W_full[c]), c)
+        if f_ids[0] in c:
+            assert r_ids[0] == f_ids[0] and r_ml[0] == f_ml[0]
+        else:
+            assert r_ml[0] <= f_ml[0]
+
+
+# ----------------------------------------------------------------------------
+# 4-bit draft head
+
+
+def run_nvfp4(vh, x, q, s, g, cand):
+    import torch
+    ids, ml = vh.mtp_draft_head_argmax_nvfp4(to_torch_bf16(x), to_torch(q), to_torch(s), g, to_torch(cand))
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), ml.cpu().numpy()
+
+
+def check_nvfp4(vh, orc, x, q, s, g, cand):
+    g_ids, g_ml = run_nvfp4(vh, x, q, s, g, cand)
+    o_ids, o_ml, o_sec = orc.draft_argmax_nvfp4(x, q, s, g, cand)
+
+    def score_of(r, gid):
+        c = int(np.searchsorted(cand, gid))
+        assert cand[c] == gid
+        return float(orc.scores_nvfp4(x[r], q[c:c + 1], s[c:c + 1], g, nthreads=1)[0])
+
+    check_ids(g_ids, g_ml, o_ids, o_ml, o_sec, score_of, TOL_4BIT)
+    return g_ids, g_ml
+
+
+def test_nvfp4_hand_worked_rows(vh):
+    """The hand-worked 4-bit rows of tests/golden/nvfp4_cases.txt, padded to
+    H = 64: checks nibble order, scale order and the tensor scale on the GPU."""
+    rows = {}
+    argmaxes = []
+    with open(os.path.join(HERE, "golden", "nvfp4_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = [p.strip() for p in line.split("|")]
+            if parts[0].startswith("row"):
+                rows[int(parts[0].split()[1])] = (bytes.fromhex(parts[1]), bytes.fromhex(parts[2]))
+            elif parts[0] == "argmax":
+                hid = {int(t.split(":")[0]): float(t.split(":")[1]) for t in parts[1].split()}
+                argmaxes.append((hid, int(parts[2])))
+    H = 64
+    q = np.zeros((3, H // 2), np.uint8)
+    s = np.zeros((3, H // 16), np.uint8)
+    for r, (qb, sb) in rows.items():
+        q[r, :16] = list(qb)
+        s[r, :2] = list(sb)
+    cand = np.array([10, 20, 30], np.int32)
+    for hid, want in argmaxes:
+        x = np.zeros((1, H), np.float32)
+        for h, v in hid.items():
+            x[0, h] = v
+        xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        g_ids, _ = run_nvfp4(vh, xb, q, s, 0.5, cand)
+        assert g_ids[0] == want
+
+
+@pytest.mark.parametrize("Vc,H,B", [(1, 64, 1), (777, 128, 1), (4097, 256, 2), (3000, 4096, 8), (1500, 1024, 11)])
+def test_nvfp4_shapes(vh, orc, syn, Vc, H, B):
+    cand = syn.sorted_subset(Vc, 2, 248_320, Vc)
+    w = syn.normal_f32(Vc, 6, (Vc, H), 0.02)
+    q, s, g = syn.nvfp4_quantize(w)
+    x = syn.normal_bf16(B, 3, (B, H), 1.0)
+    check_nvfp4(vh, orc, x, q, s, g, cand)
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_nvfp4_full_size_65536x4096(vh, orc, syn, B):
+    case = syn.nvfp4_case(Vc=65_536, H=4096, B=B, steps=3 if B == 1 else 1, seed=5)
+    for x in case.hidden:
+        check_nvfp4(vh, orc, x, case.q, case.s, case.g, case.cand_ids)
+
+
+def test_nvfp4_equals_bf16_kernel_on_representable_head(vh, orc, syn):
+    """g = 1: decoded 4-bit weights are exact bf16 values, so both kernels see
+    the same head; their ids agree outside the near-tie band."""
+    Vc, H = 6000, 512
+    rng = np.random.default_rng(3)
+    q = rng.integers(0, 256, size=(Vc, H // 2), dtype=np.uint8)
+    s = rng.integers(0x20, 0x40, size=(Vc, H // 16), dtype=np.uint8)
+    Wb = (orc.decode_nvfp4(q, s, 1.0).view(np.uint32) >> 16).astype(np.uint16)
+    cand = np.arange(Vc, dtype=np.int32) * 2
+    x = syn.normal_bf16(5, 3, (4, H), 1.0)
+    a_ids, a_ml = run_nvfp4(vh, x, q, s, 1.0, cand)
+    b_ids, b_ml = run_draft(vh, x, Wb, cand)
+    o_ids, o_ml, o_sec = orc.draft_argmax(x, Wb, cand)
+    for r in range(4):
+        if o_ml[r] - o_sec[r] > 1e-2:
+            assert a_ids[r] == b_ids[r] == o_ids[r]
+    assert np.max(np.abs(a_ml - b_ml)) < 2e-2
+
+
+# ----------------------------------------------------------------------------
+# greedy verify
+
+
+def run_verify(vh, X, W, draft, B, k, path):
+    import torch
+    acc, nid, ml = vh.spec_verify_greedy(to_torch_bf16(X), to_torch_bf16(W), to_torch(draft), B, k, path=path)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), nid.cpu().numpy(), ml.cpu().numpy()
+
+
+def check_verify(vh, orc, X, W, B, k, path, draft=None, seed=0, syn=None):
+    _, o_nid, o_ml, o_sec = orc.verify_greedy(X, W, None, B, k)
+    if draft is None:
+        draft = syn.corrupt_ids(seed, syn.STREAM_CORRUPT, o_nid.reshape(B, k + 1)[:, :k].copy(), W.shape[0], 0.45)
+    o_acc = np.array([orc.accept_len(o_nid[b * (k + 1): b * (k + 1) + k], draft[b]) for b in range(B)], np.int32)
+    g_acc, g_nid, g_ml = run_verify(vh, X, W, draft, B, k, path)
+
+    def score_of(r, v):
+        return orc.dot_bf16(X[r], W[v])
+
+    check_ids(g_nid, g_ml, o_nid, o_ml, o_sec, score_of, TOL_BF16)
+    check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
+    return g_acc, g_nid
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_verify_tiny_workload(vh, orc, syn, path):
+    _, verify, W_full = syn.tiny_case()
+    check_verify(vh, orc, verify.X, W_full, 1, 3, path, seed=1, syn=syn)
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("B,k,V,H", [(1, 1, 1000, 64), (5, 3, 1000, 128), (3, 2, 129, 192), (64, 3, 3000, 256),
+                                     (40, 3, 2049, 512), (20, 5, 700, 128), (1, 15, 517, 64)])
+def test_verify_shapes(vh, orc, syn, path, B, k, V, H):
+    W = syn.normal_bf16(V + H, 1, (V, H), 0.02)
+    X = syn.normal_bf16(B + k, 4, (B * (k + 1), H), 1.0)
+    check_verify(vh, orc, X, W, B, k, path, seed=B * 100 + k, syn=syn)
+
+
+def test_verify_more_than_256_rows(vh, orc, syn):
+    B, k, V, H = 100, 3, 1500, 128  # 400 rows: two tensor-core launches
+    W = syn.normal_bf16(77, 1, (V, H), 0.02)
+    X = syn.normal_bf16(78, 4, (B * (k + 1), H), 1.0)
+    check_verify(vh, orc, X, W, B, k, 2, seed=79, syn=syn)
+
+
+def test_verify_accept_cases(vh):
+    """Hand-built acceptance fixtures through the GPU (one-hot head)."""
+    cases = []
+    with open(os.path.join(HERE, "golden", "accept_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, nxt, dr, a, _ = [p.split() for p in line.split("|")]
+                if int(k[0]) == 3:
+                    cases.append(([int(v) for v in nxt], [int(v) for v in dr], int(a[0])))
+    B, k, H = len(cases), 3, 64
+    W = np.zeros((16, H), np.uint16)
+    for v in range(16):
+        W[v, v] = 0x3F80  # one-hot head
+    X = np.full((B * (k + 1), H), 0xBF80, np.uint16)  # -1 everywhere
+    draft = np.zeros((B, k), np.int32)
+    for b, (nxt, dr, _) in enumerate(cases):
+        for j, t in enumerate(nxt):
+            X[b * (k + 1) + j, t] = 0x4000  # 2.0 at the target id
+        draft[b] = dr
+    for path in (1, 2):
+        acc, nid, _ = run_verify(vh, X, W, draft, B, k, path)
+        assert list(acc) == [c[2] for c in cases]
+        assert list(nid) == [t for c in cases for t in c[0]]
+
+
+def _load_verify_golden():
+    path = os.path.join(HERE, "golden", "verify_b64_k3_248320x2048.txt")
+    rows, seqs, meta = {}, {}, {}
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if not p or p[0].startswith("#"):
+                continue
+            if p[0] == "row":
+                rows[int(p[1])] = (int(p[2]), float.fromhex(p[3]), float.fromhex(p[4]))
+            elif p[0] == "seq":
+                seqs[int(p[1])] = ([int(v) for v in p[2:5]], int(p[5]))
+            else:
+                meta[p[0]] = p[1:]
+    return rows, seqs, meta
+
+
+@pytest.mark.parametrize("path", [2, 1])
+def test_verify_full_size_256x248320(vh, orc, syn, path):
+    """Batched verify at full size (64 x 4 rows against the 248,320 x 2048 head)
+    against the stored oracle results, plus the live oracle on sampled rows."""
+    rows, seqs, meta = _load_verify_golden()
+    case = syn.verify_case(B=64, k=3, H=2048, V=syn.V_FULL, seed_w=2, seed=4, with_head=True)
+    assert syn.fingerprint(case.X) == int(meta["fingerprint_x"][0])
+    sample = [int(v) for v in meta["fingerprint_w_rows"][:-1]]
+    assert syn.fingerprint(np.ascontiguousarray(case.W[sample])) == int(meta["fingerprint_w_rows"][-1])
+    draft = np.array([seqs[b][0] for b in range(64)], np.int32)
+    o_nid = np.array([rows[r][0] for r in range(256)], np.int32)
+    o_ml = np.array([rows[r][1] for r in range(256)])
+    o_sec = np.array([rows[r][2] for r in range(256)])
+    o_acc = np.array([seqs[b][1] for b in range(64)], np.int32)
+    g_acc, g_nid, g_ml = run_verify(vh, case.X, case.W, draft, 64, 3, path)
+    check_ids(g_nid, g_ml, o_nid, o_ml, o_sec, lambda r, v: orc.dot_bf16(case.X[r], case.W[v]), TOL_BF16)
+    check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, 64, 3)
+    # live oracle on a few rows (independent of the stored file)
+    sample_rows = np.array([0, 37, 130, 255], np.int32)
+    _, l_nid, l_ml, _ = orc.verify_greedy(case.X, case.W, None, 64, 3, rows=sample_rows)
+    for r in sample_rows:
+        assert l_nid[r] == o_nid[r] and l_ml[r] == np.float32(o_ml[r])
+
+
+def test_cross_kernel_identity(vh, syn):
+    """Draft kernel over the identity candidate set == verify's next_ids."""
+    import torch
+    V, H, B, k = 5000, 256, 8, 3
+    W = syn.normal_bf16(31, 1, (V, H), 0.02)
+    X = syn.normal_bf16(32, 4, (B * (k + 1), H), 1.0)
+    draft = np.zeros((B, k), np.int32)
+    ids, ml = vh.mtp_draft_head_argmax(to_torch_bf16(X), to_torch_bf16(W), torch.arange(V, dtype=torch.int32,
+                                                                                          device="cuda"))
+    for path in (1, 2):
+        _, nid, vml = run_verify(vh, X, W, draft, B, k, path)
+        mism = np.nonzero(nid != ids.cpu().numpy())[0]
+        # the two kernels sum in different orders: ids may differ only on near-ties
+        for r in mism:
+            assert abs(float(vml[r]) - float(ml.cpu().numpy()[r])) < 1e-2
+
+
+def test_verify_graph_capture_replays(vh, syn):
+    """Calls are capture-safe: a CUDA graph of draft x3 + verify replays to the
+    same results as direct calls."""
+    import torch
+    case = syn.draft_case(Vc=8192, H=512, B=1, steps=3, seed=12)
+    V, B, k = 3000, 16, 3
+    Wf = to_torch_bf16(syn.normal_bf16(13, 1, (V, 512), 0.02))
+    X = to_torch_bf16(syn.normal_bf16(14, 4, (B * (k + 1), 512), 1.0))
+    d = torch.zeros((B, k), dtype=torch.int32, device="cuda")
+    Wc, cc = to_torch_bf16(case.W), to_torch(case.cand_ids)
+    xs = [to_torch_bf16(h) for h in case.hidden]
+    ws_d, ws_v = vh.workspace(1), vh.workspace(B * (k + 1))
+    ids = [torch.empty(1, dtype=torch.int32, device="cuda") for _ in range(3)]
+    mls = [torch.empty(1, dtype=torch.float32, device="cuda") for _ in range(3)]
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nid = torch.empty(B * (k + 1), dtype=torch.int32, device="cuda")
+
+    def step():
+        for i in range(3):
+            vh.mtp_draft_head_argmax(xs[i], Wc, cc, ids=ids[i], maxlogit=mls[i], ws=ws_d)
+        vh.spec_verify_greedy(X, Wf, d, B, k, accept_len=acc, next_ids=nid, ws=ws_v, want_maxlogit=False)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    want = [t.clone() for t in ids + [acc, nid]]
+    for t in ids + [acc, nid]:
+        t.fill_(-7)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        for t in ids + [acc, nid]:
+            t.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(ids + [acc, nid], want):
+            assert torch.equal(a, b)
+    assert int(ws_d.count_nonzero()) == 0 and int(ws_v.count_nonzero()) == 0
+
+
+def test_error_status_on_gpu(vh):
+    import torch
+    x = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(10, 64, dtype=torch.bfloat16, device="cuda")
+    c = torch.arange(10, dtype=torch.int32, device="cuda")
+    with pytest.raises(vh.VHError) as e:
+        vh.mtp_draft_head_argmax(x, W, c, ws=torch.zeros(8, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == vh.VH_ERR_WORKSPACE
+    flat = torch.zeros(10 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(vh.VHError) as e:
+        vh.mtp_draft_head_argmax(x, flat[8:].view(10, 64), c)  # W 16 bytes off a 32-byte boundary
+    assert e.value.status == vh.VH_ERR_ALIGN
+    with pytest.raises(vh.VHError) as e:
+        vh.spec_verify_greedy(torch.zeros(4, 80, dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros(10, 80, dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros(1, 3, dtype=torch.int32, device="cuda"), 1, 3, path=vh.VH_PATH_TENSOR)
+    assert e.value.status == vh.VH_ERR_SHAPE  # tensor path needs H % 64 == 0

@@ -1,0 +1,190 @@
+"""Python binding of libverifyhead.so (restricted-vocabulary MTP draft head and
+greedy speculative verification, GB300 / sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  If the compiled
+library is missing, every call raises: there is no fallback.
+
+Entry points mirror the C ABI in include/verifyhead.h:
+    mtp_draft_head_argmax, mtp_draft_head_argmax_nvfp4,
+    spec_verify_greedy (spec_verify_greedy_path), vh_workspace_bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libverifyhead.so")
+
+VH_OK = 0
+VH_ERR_NULL = -1
+VH_ERR_SHAPE = -2
+VH_ERR_ALIGN = -3
+VH_ERR_WORKSPACE = -4
+VH_ERR_LAUNCH = -5
+VH_ERR_DEVICE = -6
+
+VH_PATH_AUTO = 0
+VH_PATH_CUDA_CORE = 1
+VH_PATH_TENSOR = 2
+
+# Every symbol the header declares (checked by the ABI tests).
+EXPORTS = (
+    "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
+    "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
+)
+
+
+class VHError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run verify_head_gb300.build() (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.vh_version.restype = i32
+        L.vh_version.argtypes = []
+        L.vh_status_string.restype = ctypes.c_char_p
+        L.vh_status_string.argtypes = [i32]
+        L.vh_workspace_bytes.restype = sz
+        L.vh_workspace_bytes.argtypes = [i32]
+        L.mtp_draft_head_argmax.restype = i32
+        L.mtp_draft_head_argmax.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.mtp_draft_head_argmax_nvfp4.restype = i32
+        L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.spec_verify_greedy.restype = i32
+        L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.spec_verify_greedy_path.restype = i32
+        L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().vh_status_string(int(status)).decode()
+
+
+def vh_workspace_bytes(rows: int) -> int:
+    return int(lib().vh_workspace_bytes(int(rows)))
+
+
+def _check(status: int, where: str):
+    if status != VH_OK:
+        raise VHError(status, where)
+
+
+# ----------------------------------------------------------------------------
+# torch-facing helpers (device memory and streams only).
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("verify_head_gb300 takes CUDA tensors only")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (row-major)")
+
+
+def workspace(rows: int, device=None):
+    """A zeroed workspace for calls producing up to `rows` argmax rows."""
+    torch = _torch()
+    return torch.zeros(vh_workspace_bytes(rows), dtype=torch.uint8, device=device or "cuda")
+
+
+def mtp_draft_head_argmax(hidden, W_cand, cand_ids, ids=None, maxlogit=None, ws=None, stream=None):
+    """hidden [B,H] bf16, W_cand [Vc,H] bf16, cand_ids [Vc] int32 -> (ids [B] int32, maxlogit [B] fp32)."""
+    torch = _torch()
+    _require_cuda(hidden, W_cand, cand_ids)
+    B, H = hidden.shape
+    Vc = W_cand.shape[0]
+    if W_cand.shape[1] != H or cand_ids.numel() != Vc or hidden.element_size() != 2 or W_cand.element_size() != 2:
+        raise ValueError("shape/dtype mismatch")
+    if ids is None:
+        ids = torch.empty(B, dtype=torch.int32, device=hidden.device)
+    if maxlogit is None:
+        maxlogit = torch.empty(B, dtype=torch.float32, device=hidden.device)
+    if ws is None:
+        ws = workspace(B, hidden.device)
+    st = lib().mtp_draft_head_argmax(_ptr(hidden), _ptr(W_cand), _ptr(cand_ids), B, H, Vc, _ptr(ids), _ptr(maxlogit),
+                                     _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(st, "mtp_draft_head_argmax")
+    return ids, maxlogit
+
+
+def mtp_draft_head_argmax_nvfp4(hidden, Wq, scales, tensor_scale, cand_ids, ids=None, maxlogit=None, ws=None,
+                                stream=None):
+    """hidden [B,H] bf16, Wq [Vc,H/2] uint8, scales [Vc,H/16] uint8 (E4M3), tensor_scale float."""
+    torch = _torch()
+    _require_cuda(hidden, Wq, scales, cand_ids)
+    B, H = hidden.shape
+    Vc = Wq.shape[0]
+    if Wq.shape[1] * 2 != H or tuple(scales.shape) != (Vc, H // 16) or cand_ids.numel() != Vc:
+        raise ValueError("shape mismatch")
+    if ids is None:
+        ids = torch.empty(B, dtype=torch.int32, device=hidden.device)
+    if maxlogit is None:
+        maxlogit = torch.empty(B, dtype=torch.float32, device=hidden.device)
+    if ws is None:
+        ws = workspace(B, hidden.device)
+    st = lib().mtp_draft_head_argmax_nvfp4(_ptr(hidden), _ptr(Wq), _ptr(scales), float(tensor_scale), _ptr(cand_ids),
+                                           B, H, Vc, _ptr(ids), _ptr(maxlogit), _ptr(ws), ws.numel(),
+                                           _stream_ptr(stream))
+    _check(st, "mtp_draft_head_argmax_nvfp4")
+    return ids, maxlogit
+
+
+def spec_verify_greedy(hidden, W_full, draft_ids, B: int, k: int, accept_len=None, next_ids=None, row_maxlogit=None,
+                       ws=None, stream=None, path: int = VH_PATH_AUTO, want_maxlogit: bool = True):
+    """hidden [B*(k+1),H] bf16, W_full [V,H] bf16, draft_ids [B,k] int32
+    -> (accept_len [B], next_ids [B*(k+1)], row_maxlogit [B*(k+1)] or None)."""
+    torch = _torch()
+    _require_cuda(hidden, W_full, draft_ids)
+    R, H = hidden.shape
+    V = W_full.shape[0]
+    if R != B * (k + 1) or W_full.shape[1] != H or draft_ids.numel() != B * k:
+        raise ValueError("shape mismatch")
+    dev = hidden.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_ids is None:
+        next_ids = torch.empty(R, dtype=torch.int32, device=dev)
+    if row_maxlogit is None and want_maxlogit:
+        row_maxlogit = torch.empty(R, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(R, dev)
+    st = lib().spec_verify_greedy_path(_ptr(hidden), _ptr(W_full), _ptr(draft_ids), B, k, H, V, _ptr(accept_len),
+                                       _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws), ws.numel(), _stream_ptr(stream),
+                                       int(path))
+    _check(st, "spec_verify_greedy")
+    return accept_len, next_ids, row_maxlogit

@@ -1,0 +1,178 @@
+// C ABI of libverifyhead.so: host-side argument checks and kernel dispatch.
+// Declarations and the contract of every entry point: include/verifyhead.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/verifyhead.h"
+#include "vh_kernels.h"
+
+namespace {
+
+constexpr int kGemvRows = 8;   // hidden rows per CUDA-core launch
+constexpr int kTcRows = 256;   // hidden rows per tensor-core launch
+constexpr int kMaxDraftB = 256;
+constexpr int kMaxH = 65536;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Hidden rows per CUDA-core launch: up to 8, fewer when the staged hidden
+// rows (rows x H bf16 in shared memory) would exceed 128 KiB.
+inline int gemv_group(int H) {
+    int g = kGemvRows;
+    while (g > 1 && (size_t)g * H * 2 > 131072) g /= 2;
+    return g;
+}
+
+vh_status check_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return VH_ERR_DEVICE;
+    }
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess || major < 10) {
+        cudaGetLastError();
+        return VH_ERR_DEVICE;
+    }
+    return VH_OK;
+}
+
+vh::Workspace make_ws(void* ws, int rows) {
+    vh::Workspace w;
+    w.keys = static_cast<unsigned long long*>(ws);
+    w.ticket = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + vh::ws_keys_bytes(rows));
+    return w;
+}
+
+vh_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return VH_OK;
+    cudaGetLastError();  // clear a non-sticky launch error
+    return VH_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int vh_version(void) { return 10000; }
+
+const char* vh_status_string(int status) {
+    switch (status) {
+        case VH_OK: return "ok";
+        case VH_ERR_NULL: return "a required pointer is NULL";
+        case VH_ERR_SHAPE: return "a size is out of range or not a required multiple";
+        case VH_ERR_ALIGN: return "a pointer is not aligned as required";
+        case VH_ERR_WORKSPACE: return "workspace smaller than vh_workspace_bytes(rows)";
+        case VH_ERR_LAUNCH: return "CUDA launch error";
+        case VH_ERR_DEVICE: return "no usable CUDA device (sm_100 family required)";
+        default: return "unknown status";
+    }
+}
+
+size_t vh_workspace_bytes(int rows) {
+    if (rows < 1) return 0;
+    return vh::ws_total_bytes(rows);
+}
+
+vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const int32_t* cand_ids, int B, int H,
+                                int Vc, int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
+    if (!hidden || !W_cand || !cand_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
+    if (B < 1 || B > kMaxDraftB || H < 16 || H > kMaxH || H % 16 != 0 || Vc < 1) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(W_cand, 32) || !aligned(cand_ids, 4) || !aligned(ids, 4) ||
+        !aligned(maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    if (ws_bytes < vh_workspace_bytes(B)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, B);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const int grp = gemv_group(H);
+    for (int b0 = 0; b0 < B; b0 += grp) {
+        const int nb = std::min(grp, B - b0);
+        cudaError_t e = vh::launch_gemv_bf16(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
+                                             cand_ids, Vc, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
+vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                      float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
+                                      int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
+    if (!hidden || !Wq || !scales || !cand_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
+    if (B < 1 || B > kMaxDraftB || H < 64 || H > kMaxH || H % 64 != 0 || Vc < 1) return VH_ERR_SHAPE;
+    if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.0e38f)) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(Wq, 32) || !aligned(scales, 16) || !aligned(cand_ids, 4) ||
+        !aligned(ids, 4) || !aligned(maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    if (ws_bytes < vh_workspace_bytes(B)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, B);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const int grp = gemv_group(H);
+    for (int b0 = 0; b0 < B; b0 += grp) {
+        const int nb = std::min(grp, B - b0);
+        cudaError_t e = vh::launch_gemv_nvfp4(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w,
+                                              ids + b0, maxlogit + b0, s);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
+vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k,
+                                  int H, int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit,
+                                  void* ws, size_t ws_bytes, void* stream, int path) {
+    if (!hidden || !W_full || !draft_ids || !accept_len || !next_ids || !ws) return VH_ERR_NULL;
+    if (B < 1 || k < 1 || k > 15 || H < 16 || H > kMaxH || H % 16 != 0 || V < 1) return VH_ERR_SHAPE;
+    if ((long long)B * (k + 1) > 65536) return VH_ERR_SHAPE;
+    if (path != VH_PATH_AUTO && path != VH_PATH_CUDA_CORE && path != VH_PATH_TENSOR) return VH_ERR_SHAPE;
+    if (path == VH_PATH_TENSOR && H % 64 != 0) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(W_full, 32) || !aligned(draft_ids, 4) || !aligned(accept_len, 4) ||
+        !aligned(next_ids, 4) || !aligned(row_maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    const int R = B * (k + 1);
+    if (ws_bytes < vh_workspace_bytes(R)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, R);
+    const uint16_t* X = static_cast<const uint16_t*>(hidden);
+    const uint16_t* W = static_cast<const uint16_t*>(W_full);
+
+    bool tensor = (path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && R > kGemvRows && H % 64 == 0);
+    const int group = tensor ? kTcRows : gemv_group(H);
+    for (int r0 = 0; r0 < R; r0 += group) {
+        const int nr = std::min(group, R - r0);
+        vh::AcceptTail tail;
+        if (r0 + nr == R) {  // the final group also runs the acceptance scan
+            tail.draft = draft_ids;
+            tail.next_ids = next_ids;
+            tail.accept_len = accept_len;
+            tail.B = B;
+            tail.k = k;
+        }
+        float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
+        cudaError_t e;
+        if (tensor) {
+            e = vh::launch_verify_tc(X + (size_t)r0 * H, nr, H, W, V, w, next_ids + r0, ml, tail, s);
+        } else {
+            e = vh::launch_gemv_bf16(X + (size_t)r0 * H, nr, H, W, nullptr, V, w, next_ids + r0, ml, tail, s);
+        }
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
+vh_status spec_verify_greedy(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k, int H,
+                             int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
+                             size_t ws_bytes, void* stream) {
+    return spec_verify_greedy_path(hidden, W_full, draft_ids, B, k, H, V, accept_len, next_ids, row_maxlogit, ws,
+                                   ws_bytes, stream, VH_PATH_AUTO);
+}
+
+}  // extern "C"

@@ -1,0 +1,462 @@
+// Greedy verification on the 5th-generation tensor cores (tcgen05 + TMEM +
+// TMA): skinny GEMM S = W_full · Xᵀ fused with the per-hidden-row argmax
+// and the accepted-prefix scan.
+//
+// Method: the target keeps the full 248,320-row output head and verifies the
+// draft ("少读一张大表，草稿路径才真正快起来"); greedy verification accepts the
+// leading draft tokens that equal the target's own choice ("长上下文推理优化"
+// §5: MTP proposal -> target verification -> accept several tokens).
+//
+// Mapping.  One persistent CTA per SM walks 128-row tiles of W (tile t,
+// t + grid, ...).  For each tile the MMA computes D[128 W rows][N] with
+// A = W tile (M = 128, K-major) and B = all R <= 256 hidden rows (N = R
+// rounded up to 16, K-major), K = H in stages of 64 (one 128-byte swizzle
+// atom).  D lives in TMEM; two accumulator buffers of 256 columns let the
+// epilogue of tile i overlap the MMAs of tile i+1.  Scores never leave the
+// SM: the epilogue reads 32 columns at a time (thread = W row, register =
+// hidden row), packs (score, id) keys and reduces over the 32 W rows of its
+// warp with a 5-step transpose-reduce, so lane j ends up owning hidden row
+// g*32 + j.  Running maxima stay in registers across tiles; at the end the
+// four epilogue warps merge in shared memory and publish one atomicMax per
+// hidden row; the last CTA (ticket) decodes ids, runs the acceptance scan
+// and re-zeroes the workspace.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
+// MMA issuer, warps 2..5 = epilogue (TMEM lane quarter = warp % 4).
+//
+// Every wait is bounded (about 2 s of %globaltimer); on expiry the waiting
+// thread sets the workspace error word, skips the rest of its work, and the
+// CTA still drains its copies, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "vh_kernels.h"
+
+namespace vh {
+namespace tc {
+
+constexpr int kBlockM = 128;      // W rows per tile (MMA M)
+constexpr int kBlockK = 64;       // K per stage (one 128 B swizzle atom of bf16)
+constexpr int kMaxN = 256;        // hidden rows per launch (MMA N <= 256)
+constexpr int kStages = 4;
+constexpr int kThreadsTc = 192;
+constexpr int kEpiWarp0 = 2;
+constexpr int kStageA = kBlockM * kBlockK * 2;  // 16 KiB
+constexpr int kStageB = kMaxN * kBlockK * 2;    // 32 KiB
+constexpr int kTmemCols = 512;                  // two 256-column accumulators
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+struct alignas(8) Barriers {
+    unsigned long long full[kStages];
+    unsigned long long empty[kStages];
+    unsigned long long tmem_full[2];
+    unsigned long long tmem_empty[2];
+    unsigned long long mma_done;
+    unsigned int tmem_base;
+    unsigned int pad;
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB) + sizeof(Barriers) +
+                              kMaxN * 8 /*merge*/ + 64;
+
+struct TcArgs {
+    int R;        // hidden rows in this launch (1..256)
+    int N;        // MMA N = R rounded up to 16
+    int H;
+    int V;
+    int n_tiles;  // ceil(V / 128)
+    Workspace ws;
+    unsigned int* err;
+    int32_t* next_ids;
+    float* maxlogit;
+    AcceptTail tail;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a barrier phase.  Returns false (and raises the error word)
+// if the phase does not complete within the time limit or an error is
+// already raised.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(err, 1u);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the error word (used to drain in-flight work
+// before the CTA releases its shared memory and TMEM).
+__device__ __forceinline__ void mbar_drain(unsigned long long* bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, unsigned long long* bar, int x, int y,
+                                            unsigned long long policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ unsigned long long policy_evict_first() {
+    unsigned long long p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ unsigned long long policy_evict_last() {
+    unsigned long long p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), tile base 1024-byte aligned.
+__device__ __forceinline__ unsigned long long smem_desc_sw128(uint32_t saddr) {
+    unsigned long long d = 0;
+    d |= (unsigned long long)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (unsigned long long)(16u >> 4) << 16;                   // leading byte offset (unused here)
+    d |= (unsigned long long)(1024u >> 4) << 32;                 // stride byte offset
+    d |= 1ull << 46;                                             // descriptor version (tcgen05)
+    d |= 2ull << 61;                                             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4)                     // D format: f32
+           | (1u << 7)                   // A format: bf16
+           | (1u << 10)                  // B format: bf16
+           | ((uint32_t)(N >> 3) << 17)  // N / 8
+           | ((uint32_t)(M >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, unsigned long long adesc, unsigned long long bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(unsigned long long* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 columns of fp32 from TMEM: thread t gets lane (base + t),
+// columns col .. col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+// Transpose-reduce: v[j] is this lane's key for column j; afterwards lane j
+// holds the maximum over all 32 lanes of column j (returned).
+__device__ __forceinline__ unsigned long long transpose_max32(unsigned long long (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const unsigned long long send = upper ? v[i] : v[i + s];
+            const unsigned long long keep = upper ? v[i + s] : v[i];
+            const unsigned long long recv = __shfl_xor_sync(0xFFFFFFFFu, send, s);
+            v[i] = umax64(keep, recv);
+        }
+    }
+    return v[0];
+}
+
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    k_verify_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x, const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_a = smem;                                  // kStages x 16 KiB (W tiles)
+    uint8_t* stage_b = smem + (size_t)kStages * kStageA;      // kStages x 32 KiB (hidden rows)
+    Barriers* bars = reinterpret_cast<Barriers*>(stage_b + (size_t)kStages * kStageB);
+    unsigned long long* merge = reinterpret_cast<unsigned long long*>(bars + 1);  // [kMaxN]
+    __shared__ unsigned int s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k_stages = a.H / kBlockK;
+    const uint32_t b_bytes = (uint32_t)a.N * kBlockK * 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->tmem_full[b], 1);
+            mbar_init(&bars->tmem_empty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(&bars->mma_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < kMaxN; i += blockDim.x) merge[i] = 0ull;
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars->tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const unsigned long long pol_w = policy_evict_first();
+            const unsigned long long pol_x = policy_evict_last();
+            uint32_t it = 0;  // global k-stage counter
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.n_tiles && ok; tile += gridDim.x) {
+                for (int ks = 0; ks < k_stages; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait(&bars->empty[s], ph ^ 1u, a.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bars->full[s], (uint32_t)kStageA + b_bytes);
+                    tma_load_2d(stage_a + (size_t)s * kStageA, &map_w, &bars->full[s], ks * kBlockK,
+                                tile * kBlockM, pol_w);
+                    tma_load_2d(stage_b + (size_t)s * kStageB, &map_x, &bars->full[s], ks * kBlockK, 0, pol_x);
+                }
+            }
+            // drain: every issued load must land before the CTA may exit
+            const uint32_t issued = it;
+            for (uint32_t j = (issued > (uint32_t)kStages ? issued - kStages : 0); j < issued; ++j)
+                mbar_drain(&bars->full[j % kStages], (j / kStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kBlockM, a.N);
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.n_tiles && ok; tile += gridDim.x, ++local) {
+                const uint32_t buf = local & 1u;
+                if (!mbar_wait(&bars->tmem_empty[buf], ((local >> 1) & 1u) ^ 1u, a.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * 256u;
+                for (int ks = 0; ks < k_stages; ++ks, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(&bars->full[s], (it / kStages) & 1u, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(stage_a + (size_t)s * kStageA);
+                    const uint32_t sb = smem_u32(stage_b + (size_t)s * kStageB);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                        mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
+                                 (ks > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars->empty[s]);
+                }
+                if (ok) mma_commit(&bars->tmem_full[buf]);
+            }
+            // all MMAs issued by this thread have completed once this arrives
+            mma_commit(&bars->mma_done);
+            mbar_drain(&bars->mma_done, 0u);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;  // TMEM lanes quarter*32 .. +31
+        const int ngroups = (a.N + 31) / 32;
+        unsigned long long best[kMaxN / 32];
+#pragma unroll
+        for (int g = 0; g < kMaxN / 32; ++g) best[g] = 0ull;
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++local) {
+            const uint32_t buf = local & 1u;
+            if (!mbar_wait(&bars->tmem_full[buf], (local >> 1) & 1u, a.err)) break;
+            tc_fence_after();
+            const int row = tile * kBlockM + quarter * 32 + lane;  // this thread's W row (global id)
+            const bool valid = row < a.V;
+#pragma unroll
+            for (int g = 0; g < kMaxN / 32; ++g) {
+                if (g < ngroups) {
+                    float v[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 256u + g * 32u, v);
+                    unsigned long long key[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) key[j] = valid ? make_key(v[j], (uint32_t)row) : 0ull;
+                    best[g] = umax64(best[g], transpose_max32(key));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxN / 32; ++g)
+            if (g < ngroups && best[g] != 0ull) atomicMax(&merge[g * 32 + lane], best[g]);
+    }
+
+    // ---------------- CTA merge, publish, last-CTA decode ----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x)
+        if (merge[r] != 0ull) atomicMax(a.ws.keys + r, merge[r]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+        const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
+        a.next_ids[r] = (int32_t)key_gid(k);
+        if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
+    }
+    if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
+    if (a.tail.draft != nullptr) {
+        __threadfence();
+        __syncthreads();
+        const int k = a.tail.k;
+        for (int b = threadIdx.x; b < a.tail.B; b += blockDim.x) {
+            const volatile int32_t* nid = a.tail.next_ids + (size_t)b * (k + 1);
+            const int32_t* d = a.tail.draft + (size_t)b * k;
+            int acc = 0;
+            while (acc < k && nid[acc] == d[acc]) ++acc;
+            a.tail.accept_len[b] = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps through the driver entry point (no libcuda link).
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 row-major [rows][H] map with a [box_rows][64] box, 128 B swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int rows, int H, int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
+                             int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    using namespace tc;
+    if (R < 1 || R > kMaxN || H < kBlockK || H % kBlockK != 0 || V < 1) return cudaErrorNotSupported;
+    const int N = (R + 15) / 16 * 16;
+    alignas(64) CUtensorMap map_w, map_x;
+    if (!make_map(&map_w, W, V, H, kBlockM) || !make_map(&map_x, X, R, H, N)) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(k_verify_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    TcArgs a{};
+    a.R = R;
+    a.N = N;
+    a.H = H;
+    a.V = V;
+    a.n_tiles = (V + kBlockM - 1) / kBlockM;
+    a.ws = ws;
+    a.err = ws.ticket + 1;
+    a.next_ids = next_ids;
+    a.maxlogit = maxlogit;
+    a.tail = tail;
+    const int grid = std::max(1, std::min(sm_count(), a.n_tiles));
+    k_verify_tc<<<grid, kThreadsTc, kSmemBytes, s>>>(map_w, map_x, a);
+    return cudaGetLastError();
+}
+
+}  // namespace vh

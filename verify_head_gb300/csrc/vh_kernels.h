@@ -1,0 +1,40 @@
+// Internal launchers behind the C ABI (not part of the public interface).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vh_common.cuh"
+
+namespace vh {
+
+// Optional acceptance scan run by the last CTA of a launch, after the group's
+// argmax ids are written: accept_len[b] = leading j < k with
+// next_ids[b*(k+1)+j] == draft[b*k+j], over all B sequences.
+struct AcceptTail {
+    const int32_t* draft = nullptr;  // [B][k]; nullptr = no scan
+    const int32_t* next_ids = nullptr;  // [B*(k+1)], complete once this launch ends
+    int32_t* accept_len = nullptr;   // [B]
+    int B = 0;
+    int k = 0;
+};
+
+// bf16 streaming GEMV + argmax over rows [0, n_rows) of W for nb <= 8 hidden
+// rows.  gid of row r is cand[r] (cand != nullptr) or r.
+cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                             Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+
+// Block-scaled 4-bit (E2M1 codes, E4M3 block scales, fp32 tensor scale)
+// GEMV + argmax on CUDA cores, nb <= 8.
+cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
+                              const int32_t* cand, int n_rows, Workspace ws, int32_t* ids, float* maxlogit,
+                              cudaStream_t s);
+
+// tcgen05 skinny GEMM + per-row argmax + acceptance scan for R <= 256 hidden
+// rows (H % 64 == 0).  Returns cudaErrorNotSupported when the shape does not
+// fit the kernel.
+cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
+                             int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+
+int sm_count();
+
+}  // namespace vh
