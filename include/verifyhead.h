@@ -146,6 +146,37 @@ VH_API vh_status spec_verify_greedy(const void* hidden, const void* W_full, cons
                              int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
                              size_t ws_bytes, void* stream);
 
+/*
+ * mtp_draft_head_argmax without a caller workspace (no counterpart in the
+ * source pages; an interface addition).
+ *
+ * For callers that cannot allocate device memory or pass a workspace: e.g.
+ * an engine's per-step execute hook or plugin interface that gives extensions
+ * no allocator, or a decode loop with a fixed memory plan, where cudaMalloc
+ * may synchronise the device or fail mid-step.  Results are those of
+ * mtp_draft_head_argmax with the same arguments.
+ *
+ * Scratch is a fixed 4 KiB device array inside this library, on every device
+ * that loads it, kept until the process exits.  Limit: B <= 256 hidden rows
+ * per call; a larger B returns VH_ERR_WORKSPACE and launches nothing.  The
+ * call allocates and frees nothing.  It clears the part of the array it uses
+ * (cudaMemsetAsync on `stream`) before the kernel, because the array keeps
+ * whatever the previous call left.
+ *
+ * All calls on one device share that single array: calls that can overlap
+ * on the GPU (different streams without ordering, several host threads)
+ * race and may return wrong ids.  Keep such calls in one stream.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.
+ *
+ * Arguments as for mtp_draft_head_argmax, without ws / ws_bytes.
+ */
+VH_API vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand, const int32_t* cand_ids,
+                                                 int B, int H, int Vc, int32_t* ids, float* maxlogit,
+                                                 void* stream);
+
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
     VH_PATH_AUTO = 0,      /* tensor cores when B*(k+1) > 8 and H % 64 == 0, else CUDA cores */

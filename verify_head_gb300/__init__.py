@@ -33,6 +33,7 @@ VH_PATH_TENSOR = 2
 EXPORTS = (
     "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
+    "mtp_draft_head_argmax_static_ws",
 )
 
 
@@ -70,6 +71,8 @@ def lib():
         L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
         L.spec_verify_greedy.restype = i32
         L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.mtp_draft_head_argmax_static_ws.restype = i32
+        L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.spec_verify_greedy_path.restype = i32
         L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
         _lib = L

@@ -67,7 +67,7 @@ struct Workspace {
     unsigned int* ticket;
 };
 
-__host__ __device__ inline size_t ws_keys_bytes(int rows) { return ((size_t)rows * 8 + 15) / 16 * 16; }
-__host__ __device__ inline size_t ws_total_bytes(int rows) { return ws_keys_bytes(rows) + 16; }
+__host__ __device__ constexpr size_t ws_keys_bytes(int rows) { return ((size_t)rows * 8 + 15) / 16 * 16; }
+__host__ __device__ constexpr size_t ws_total_bytes(int rows) { return ws_keys_bytes(rows) + 16; }
 
 }  // namespace vh
