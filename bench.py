@@ -288,7 +288,7 @@ def run_ours(args):
     del W
 
     extra = {}
-    if rank == 0 and not args.skip_extra:
+    if rank == 0 and not args.skip_extra and args.workload == "all":
         extra = measure_extra(torch, vh, synth, timer, peaks, load_verify_golden)
 
     cpu = None
@@ -323,7 +323,19 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
+def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"):
+    dev = torch.device("cuda")
+    out = {}
+    if only in ("all", "verify"):
+        out.update(measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=(only == "all")))
+    if only in ("all", "sweep"):
+        out["sweep"] = measure_sweep(torch, vh, synth, timer, peaks)
+    if only in ("all", "nvfp4"):
+        out["nvfp4"] = measure_nvfp4(torch, vh, synth, timer, peaks)
+    return out
+
+
+def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=True):
     dev = torch.device("cuda")
     out = {}
 
@@ -340,7 +352,8 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
     acc = torch.empty(64, dtype=torch.int32, device=dev)
     nid = torch.empty(256, dtype=torch.int32, device=dev)
     ml = torch.empty(256, dtype=torch.float32, device=dev)
-    for path, name in ((vh.VH_PATH_TENSOR, "verify"), (vh.VH_PATH_CUDA_CORE, "verify_cuda_core")):
+    paths = [(vh.VH_PATH_TENSOR, "verify")] + ([(vh.VH_PATH_CUDA_CORE, "verify_cuda_core")] if cuda_core else [])
+    for path, name in paths:
         us = timer.time_calls(lambda: vh.spec_verify_greedy(X, Wf, draft, 64, 3, accept_len=acc, next_ids=nid,
                                                             row_maxlogit=ml, ws=ws, path=path),
                               5 if path == vh.VH_PATH_TENSOR else 2, warmup=2 if path == vh.VH_PATH_TENSOR else 1)
@@ -361,8 +374,15 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
             "gpu_launches_per_round": 1 if path == vh.VH_PATH_TENSOR else 32,
         }
     del Wf, X
+    return out
 
-    # ---- head-size sweep, B=1 ----
+
+def measure_sweep(torch, vh, synth, timer, peaks):
+    dev = torch.device("cuda")
+
+    def t_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
     sweep = {}
     for Vc in (248_320, 65_536, 32_768):
         c = synth.draft_case(Vc=Vc, H=2048, B=1, steps=1, seed=2, cand_seed=3)
@@ -377,9 +397,15 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
                           "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
                           "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
         del Wc
-    out["sweep"] = sweep
+    return sweep
 
-    # ---- block-scaled 4-bit head 65,536 x 4096, B = 1 and 8 ----
+
+def measure_nvfp4(torch, vh, synth, timer, peaks):
+    dev = torch.device("cuda")
+
+    def t_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
     nv = {}
     for B in (1, 8):
         c = synth.nvfp4_case(Vc=65_536, H=4096, B=B, steps=1, seed=5)
@@ -394,8 +420,19 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden):
         nv[f"B{B}"] = {"steps_per_s": round(1e6 / med, 1), **stats(us),
                        "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
                        "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
-    out["nvfp4"] = nv
-    return out
+    return nv
+
+
+def run_single(args):
+    """One of the extra measurements on its own (a short profiling target)."""
+    import torch
+    import synth
+    import verify_head_gb300 as vh
+    vh.lib()
+    peaks, _ = load_peaks()
+    timer = Timer(torch)
+    out = measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only=args.workload)
+    print(json.dumps(out), flush=True)
 
 
 def cpu_baseline(case, seconds: float = 10.0):
@@ -455,9 +492,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
+    ap.add_argument("--workload", default="all", choices=["all", "draft", "verify", "sweep", "nvfp4"],
+                    help="all = the bench line; others run one measurement only (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.impl == "ours" and args.workload not in ("all", "draft"):
+        run_single(args)
+        return
     if args.impl == "reference":
         args.steps = max(1, min(args.steps, 50))  # bounded: ~0.1-0.5 s of CPU per draft step
         run_reference(args)
