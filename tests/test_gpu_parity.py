@@ -70,7 +70,8 @@ def test_tiny_workload(vh, orc, syn):
 
 @pytest.mark.parametrize("Vc,H,B", [(1, 16, 1), (7, 64, 1), (1023, 256, 1), (1024, 256, 2), (1025, 272, 3),
                                     (5000, 2048, 1), (3001, 2080, 5), (2500, 4096, 8), (700, 6144, 9),
-                                    (4099, 128, 17)])
+                                    (4099, 128, 17), (33, 4096, 1), (100_003, 2048, 1), (9000, 1040, 1),
+                                    (500, 8192, 1)])
 def test_draft_shapes(vh, orc, syn, Vc, H, B):
     cand = syn.sorted_subset(Vc + H, 2, 300_000, Vc)
     W = syn.normal_bf16(Vc + 7, 1, (Vc, H), 0.02)
@@ -208,7 +209,8 @@ def test_nvfp4_hand_worked_rows(vh):
         assert g_ids[0] == want
 
 
-@pytest.mark.parametrize("Vc,H,B", [(1, 64, 1), (777, 128, 1), (4097, 256, 2), (3000, 4096, 8), (1500, 1024, 11)])
+@pytest.mark.parametrize("Vc,H,B", [(1, 64, 1), (777, 128, 1), (4097, 256, 2), (3000, 4096, 8), (1500, 1024, 11),
+                                    (1, 256, 1), (5003, 256, 1), (3001, 1024, 1), (999, 8192, 1), (40_000, 4096, 1)])
 def test_nvfp4_shapes(vh, orc, syn, Vc, H, B):
     cand = syn.sorted_subset(Vc, 2, 248_320, Vc)
     w = syn.normal_f32(Vc, 6, (Vc, H), 0.02)

@@ -21,6 +21,7 @@
 #include <algorithm>
 
 #include "vh_kernels.h"
+#include "vh_ptx.cuh"
 
 namespace vh {
 
@@ -34,6 +35,12 @@ struct GemvArgs {
     int H;
     int n_rows;
     int rows_per_warp;
+    // bulk-copy ring kernels only
+    int rows_per_cta;
+    int rows_per_stage;  // multiple of kRingConsumers
+    int stage_bytes;
+    int n_stages;
+    unsigned int* err;
     Workspace ws;
     int32_t* ids;
     float* maxlogit;
@@ -46,6 +53,16 @@ __device__ __forceinline__ U32x8 ld_x32(const uint16_t* p) {
     U32x8 r;
     r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
     r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
+    return r;
+}
+
+// 32 bytes from shared memory (address in the shared window).
+__device__ __forceinline__ U32x8 lds32(uint32_t saddr) {
+    U32x8 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "r"(saddr));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7]) : "r"(saddr + 16));
     return r;
 }
 
@@ -66,9 +83,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Merge per-warp best keys, publish with atomicMax, and let the last CTA
 // decode, run the optional acceptance scan and reset the workspace.
-template <int NB>
-__device__ __forceinline__ void finish_argmax(const unsigned long long (&best)[NB], const GemvArgs& a) {
-    __shared__ unsigned long long red[kWarps][NB];
+template <int NB, int NW = kWarps, typename Args>
+__device__ __forceinline__ void finish_argmax(const unsigned long long (&best)[NB], const Args& a) {
+    __shared__ unsigned long long red[NW][NB];
     __shared__ unsigned int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
@@ -79,7 +96,7 @@ __device__ __forceinline__ void finish_argmax(const unsigned long long (&best)[N
     if (threadIdx.x < a.nb) {
         unsigned long long k = 0;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) k = red[w][threadIdx.x] > k ? red[w][threadIdx.x] : k;
+        for (int w = 0; w < NW; ++w) k = red[w][threadIdx.x] > k ? red[w][threadIdx.x] : k;
         if (k != 0) atomicMax(a.ws.keys + threadIdx.x, k);
     }
     __threadfence();
@@ -110,15 +127,34 @@ __device__ __forceinline__ void finish_argmax(const unsigned long long (&best)[N
 
 // ---------------------------------------------------------------------------
 // bf16 head.  x is staged in shared memory as bf16 (read once per chunk and
-// shared by the two rows in flight); the row is walked in segments of 2048
-// elements (four 32-byte chunks per lane).
+// shared by the rows in flight); the row is walked in segments of 2048
+// elements (four 32-byte chunks per lane).  RPI rows per warp iteration.
+//
+// Programmatic dependent launch: the kernel lets the next kernel in the
+// stream launch at once, prefetches its first rows into L2 (read-only
+// weights), and only then waits for the previous kernel to finish, before
+// it touches x or the workspace.
 
-template <int NB>
-__global__ void __launch_bounds__(kThreads, (NB == 1 ? 2 : 1)) k_gemv_bf16(const GemvArgs a) {
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+template <int NB, int RPI>
+__global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const GemvArgs a) {
     extern __shared__ __align__(16) uint16_t xs[];  // [NB][H]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = a.H, nch = H >> 4;  // 32-byte chunks per row
     const uint16_t* __restrict__ W = static_cast<const uint16_t*>(a.W);
+
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long r0 = gw * a.rows_per_warp;
+    const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
+
+    pdl_launch_dependents();
+    for (long long r = r0; r < min(r1, r0 + RPI); ++r)
+        for (int c = lane; c < min(nch, 128); c += 32) prefetch_l2(W + (size_t)r * H + c * 16);
+    pdl_wait();
 
     {
         const int n16 = NB * H / 8;
@@ -135,25 +171,21 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 2 : 1)) k_gemv_bf16(const
 #pragma unroll
     for (int b = 0; b < NB; ++b) best[b] = 0ull;
 
-    const long long gw = (long long)blockIdx.x * kWarps + warp;
-    const long long r0 = gw * a.rows_per_warp;
-    const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
-
-    for (long long r = r0; r < r1; r += 2) {
-        const bool two = (r + 1 < r1);
+    for (long long r = r0; r < r1; r += RPI) {
+        const bool two = RPI > 1 && (r + 1 < r1);
         const uint16_t* w0p = W + (size_t)r * H;
         const uint16_t* w1p = w0p + H;
         float p0[NB][2], p1[NB][2];
 #pragma unroll
         for (int b = 0; b < NB; ++b) p0[b][0] = p0[b][1] = p1[b][0] = p1[b][1] = 0.f;
         for (int seg = 0; seg < nch; seg += 128) {
-            U32x8 w0[4], w1[4];
+            U32x8 w0[4], w1[RPI > 1 ? 4 : 1];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int c = seg + lane + 32 * i;
                 if (c < nch) {
                     w0[i] = ld_stream32(w0p + c * 16);
-                    if (two) w1[i] = ld_stream32(w1p + c * 16);
+                    if (two) w1[RPI > 1 ? i : 0] = ld_stream32(w1p + c * 16);
                 }
             }
 #pragma unroll
@@ -164,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 2 : 1)) k_gemv_bf16(const
                     for (int b = 0; b < NB; ++b) {
                         const U32x8 xv = ld_x32(xs + (size_t)b * H + c * 16);
                         dot16(w0[i], xv, p0[b][0], p0[b][1]);
-                        if (two) dot16(w1[i], xv, p1[b][0], p1[b][1]);
+                        if (two) dot16(w1[RPI > 1 ? i : 0], xv, p1[b][0], p1[b][1]);
                     }
                 }
             }
@@ -186,10 +218,11 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 2 : 1)) k_gemv_bf16(const
     finish_argmax<NB>(best, a);
 }
 
+
 // ---------------------------------------------------------------------------
-// Block-scaled 4-bit head on CUDA cores.  A lane chunk is 32 code bytes = 64
-// elements = 4 scale blocks.  Each 16-element block is summed unscaled, then
-// multiplied by its E4M3 scale; the tensor scale g multiplies the total.
+// Block-scaled 4-bit decoding helpers.  E2M1 pairs and E4M3 scale pairs go
+// through the hardware conversions to f16x2 (exact: every E2M1 and E4M3
+// value is an f16 value).
 
 __device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t byte) {
     uint32_t h2;
@@ -204,6 +237,221 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two_bytes) {
     __half2 h = *reinterpret_cast<__half2*>(&h2);
     return __half22float2(h);
 }
+
+// ---------------------------------------------------------------------------
+// Bulk-copy ring geometry (4-bit head, B = 1).
+
+constexpr int kRingConsumers = 8;
+constexpr int kRingThreads = (kRingConsumers + 1) * 32;
+constexpr int kRingMaxStages = 8;
+constexpr int kRingSmem = 192 * 1024;
+
+// ---------------------------------------------------------------------------
+// Block-scaled 4-bit head, B = 1, H <= 8192: bulk-copy ring (codes and scales
+// stream through two shared-memory rings).  Weights decode with one
+// cvt.rn.f16x2.e2m1x2 per byte (exact); the hidden row is held in registers
+// as f16, prescaled by a power of two 2^k so that its largest magnitude
+// lies in [2^14, 2^15) (exact for every element within 2^31 of the largest);
+// products accumulate in fp32 with the mixed-precision fma.rn.f32.f16.  Each
+// 16-element block sum is multiplied by its E4M3 scale; the total by g*2^-k.
+
+__device__ __forceinline__ void split_h2(uint32_t w, unsigned short& lo, unsigned short& hi) {
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+
+__device__ __forceinline__ float fma_f16_f32(unsigned short a, unsigned short b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+    return h2;
+}
+
+// 16-element block: codes in (q0, q1) (element 2i in the low nibble of byte
+// i), hidden row as 8 f16x2 words.  Unscaled fp32 sum.
+__device__ __forceinline__ float nvfp4_block16(uint32_t q0, uint32_t q1, const uint32_t* xh) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t w2 = e2m1x2_to_h2(((j < 4 ? q0 : q1) >> (8 * (j & 3))) & 0xFFu);
+        unsigned short wl, wh, xl, xhh;
+        split_h2(w2, wl, wh);
+        split_h2(xh[j], xl, xhh);
+        a0 = fma_f16_f32(wl, xl, a0);
+        a1 = fma_f16_f32(wh, xhh, a1);
+    }
+    return a0 + a1;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(kRingThreads, 1) k_draft_ring_nvfp4(const GemvArgs a) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) unsigned long long full[kRingMaxStages], empty[kRingMaxStages];
+    __shared__ float s_xmax[kRingConsumers];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = a.H, nch = H >> 6;  // 64-element chunks: 32 code bytes + 4 scale bytes
+    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
+    const long long row_begin = (long long)blockIdx.x * a.rows_per_cta;
+    const long long row_end = min(row_begin + (long long)a.rows_per_cta, (long long)a.n_rows);
+    const int n_iter = row_end > row_begin ? (int)((row_end - row_begin + a.rows_per_stage - 1) / a.rows_per_stage) : 0;
+    const int S = a.n_stages;
+    const uint32_t qstage = (uint32_t)(a.rows_per_stage * qrow);  // code bytes per stage
+    uint8_t* sring = ring + (size_t)S * qstage;                    // scale ring after the code ring
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kRingConsumers);
+        }
+        ptx::fence_barrier_init();
+    }
+    // largest |x| (identical in every CTA) -> power-of-two prescale 2^k
+    if (warp < kRingConsumers) {
+        float m = 0.f;
+        for (int i = warp * 32 + lane; i < H; i += kRingConsumers * 32)
+            m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) s_xmax[warp] = m;
+    }
+    __syncthreads();
+
+    unsigned long long best[1] = {0ull};
+    if (warp == kRingConsumers) {
+        if (lane == 0) {
+            const unsigned long long pol = ptx::policy_evict_first();
+            const uint8_t* Wq = static_cast<const uint8_t*>(a.W);
+            int i = 0;
+            for (; i < n_iter; ++i) {
+                const int s = i % S;
+                if (!ptx::mbar_wait(&empty[s], ((i / S) & 1) ^ 1, a.err)) break;
+                const long long r0 = row_begin + (long long)i * a.rows_per_stage;
+                const long long nr = min((long long)a.rows_per_stage, row_end - r0);
+                const uint32_t qb = (uint32_t)(nr * qrow), sb = (uint32_t)(nr * srow);
+                ptx::mbar_arrive_expect_tx(&full[s], qb + sb);
+                ptx::bulk_load(ring + (size_t)s * qstage, Wq + (size_t)r0 * qrow, qb, &full[s], pol);
+                ptx::bulk_load(sring + (size_t)s * a.rows_per_stage * srow, a.scales + (size_t)r0 * srow, sb, &full[s],
+                               pol);
+            }
+            for (int j = (i > S ? i - S : 0); j < i; ++j) ptx::mbar_drain(&full[j % S], (j / S) & 1);
+        }
+    } else {
+        float xmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < kRingConsumers; ++w) xmax = fmaxf(xmax, s_xmax[w]);
+        int k = 0;
+        if (xmax > 0.f) {
+            const int e = (int)((__float_as_uint(xmax) >> 23) & 0xFF);  // biased exponent of the largest |x|
+            k = min(127, 141 - e);                                      // largest |x| * 2^k in [2^14, 2^15)
+        }
+        const float up = ldexpf(1.f, k);
+        const float out_scale = a.g * ldexpf(1.f, -k);
+        uint32_t xh[CPL][32];  // lane's chunks of x as f16x2
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                if (c < nch) {
+                    const uint32_t pr = reinterpret_cast<const uint32_t*>(a.x)[c * 32 + t];
+                    xh[j][t] = f32x2_to_h2(bf_lo(pr) * up, bf_hi(pr) * up);
+                } else {
+                    xh[j][t] = 0u;
+                }
+            }
+        }
+        const uint32_t ring_base = ptx::smem_u32(ring), sring_base = ptx::smem_u32(sring);
+        for (int i = 0; i < n_iter; ++i) {
+            const int s = i % S;
+            if (!ptx::mbar_wait(&full[s], (i / S) & 1, a.err)) break;
+            const long long r0 = row_begin + (long long)i * a.rows_per_stage;
+            float score[4];
+            int nr = 0;
+            for (int rr = warp; rr < a.rows_per_stage && nr < 4; rr += kRingConsumers, ++nr) {
+                float acc = 0.f;
+                if (r0 + rr < row_end) {
+                    const uint32_t qaddr = ring_base + (uint32_t)s * qstage + (uint32_t)(rr * qrow);
+                    const uint32_t saddr = sring_base + (uint32_t)((s * a.rows_per_stage + rr) * srow);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        const int c = lane + 32 * j;
+                        if (c < nch) {
+                            const U32x8 q = lds32(qaddr + c * 32);
+                            uint32_t sc;
+                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(saddr + c * 4));
+                            const float2 s01 = e4m3x2_to_f2(sc & 0xFFFFu);
+                            const float2 s23 = e4m3x2_to_f2(sc >> 16);
+                            acc = fmaf(nvfp4_block16(q.v[0], q.v[1], &xh[j][0]), s01.x, acc);
+                            acc = fmaf(nvfp4_block16(q.v[2], q.v[3], &xh[j][8]), s01.y, acc);
+                            acc = fmaf(nvfp4_block16(q.v[4], q.v[5], &xh[j][16]), s23.x, acc);
+                            acc = fmaf(nvfp4_block16(q.v[6], q.v[7], &xh[j][24]), s23.y, acc);
+                        }
+                    }
+                }
+                score[nr] = acc;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[s]);
+            nr = 0;
+            for (int rr = warp; rr < a.rows_per_stage && nr < 4; rr += kRingConsumers, ++nr) {
+                const long long r = r0 + rr;
+                if (r < row_end) {
+                    const float sc = warp_sum(score[nr]) * out_scale;
+                    const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
+                    const unsigned long long kk = make_key(sc, gid);
+                    best[0] = kk > best[0] ? kk : best[0];
+                }
+            }
+        }
+    }
+    finish_argmax<1, kRingConsumers + 1>(best, a);
+}
+
+static cudaError_t launch_ring_nvfp4(GemvArgs& a, cudaStream_t s) {
+    const int H = a.H;
+    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
+    int rps = (int)std::min<size_t>(32, std::max<size_t>(kRingConsumers, (32768 / qrow) / kRingConsumers *
+                                                                            kRingConsumers));
+    a.rows_per_stage = rps;
+    a.stage_bytes = (int)(rps * (qrow + srow));
+    a.n_stages = std::min(kRingMaxStages, kRingSmem / a.stage_bytes);
+    if (a.n_stages < 2) return cudaErrorNotSupported;
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidConfiguration;
+    long long grid = std::min<long long>(sms, ((long long)a.n_rows + rps - 1) / rps);
+    a.rows_per_cta = (int)(((long long)a.n_rows + grid - 1) / grid);
+    grid = ((long long)a.n_rows + a.rows_per_cta - 1) / a.rows_per_cta;
+    const size_t smem = (size_t)a.n_stages * a.stage_bytes;
+    const int cpl = (H / 64 + 31) / 32;
+#define VH_RING4_CASE(C)                                                                                \
+    if (cpl <= C) {                                                                                      \
+        cudaError_t e = cudaFuncSetAttribute(k_draft_ring_nvfp4<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                             (int)smem);                                                 \
+        if (e != cudaSuccess) return e;                                                                  \
+        k_draft_ring_nvfp4<C><<<(unsigned)grid, kRingThreads, smem, s>>>(a);                             \
+        return cudaGetLastError();                                                                       \
+    }
+    VH_RING4_CASE(1)
+    VH_RING4_CASE(2)
+    VH_RING4_CASE(4)
+#undef VH_RING4_CASE
+    return cudaErrorNotSupported;
+}
+
+// ---------------------------------------------------------------------------
+// Block-scaled 4-bit head on CUDA cores, any B <= 8.  A lane chunk is 32 code
+// bytes = 64 elements = 4 scale blocks.  Each 16-element block is summed
+// unscaled, then multiplied by its E4M3 scale; g multiplies the total.
 
 template <int NB>
 __global__ void __launch_bounds__(kThreads) k_gemv_nvfp4(const GemvArgs a) {
@@ -301,7 +549,7 @@ int sm_count() {
 }
 
 template <typename K>
-static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a, cudaStream_t s) {
+static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a, cudaStream_t s, bool pdl) {
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -319,8 +567,17 @@ static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a
     const long long warps = grid * kWarps;
     a.rows_per_warp = (int)(((long long)n_rows + warps - 1) / warps);
     grid = ((long long)n_rows + (long long)a.rows_per_warp * kWarps - 1) / ((long long)a.rows_per_warp * kWarps);
-    kernel<<<(unsigned)grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
@@ -328,9 +585,10 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
     GemvArgs a{};
     a.x = x; a.W = W; a.scales = nullptr; a.g = 1.f; a.cand = cand;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit; a.tail = tail;
+    a.err = ws.ticket + 1;
+    if (nb == 1) return launch_split_v(k_gemv_bf16<1, 1>, (size_t)H * 2, n_rows, a, s, true);
 #define VH_GEMV_CASE(NBV) \
-    if (nb <= NBV) return launch_split_v(k_gemv_bf16<NBV>, (size_t)NBV * H * 2, n_rows, a, s);
-    VH_GEMV_CASE(1)
+    if (nb <= NBV) return launch_split_v(k_gemv_bf16<NBV, 2>, (size_t)NBV * H * 2, n_rows, a, s, true);
     VH_GEMV_CASE(2)
     VH_GEMV_CASE(4)
     VH_GEMV_CASE(8)
@@ -344,8 +602,10 @@ cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* W
     GemvArgs a{};
     a.x = x; a.W = Wq; a.scales = scales; a.g = g; a.cand = cand;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit;
+    a.err = ws.ticket + 1;
+    if (nb == 1 && H <= 8192 && H % 256 == 0) return launch_ring_nvfp4(a, s);  // scale rows of 16-byte multiples
 #define VH_NVFP4_CASE(NBV) \
-    if (nb <= NBV) return launch_split_v(k_gemv_nvfp4<NBV>, (size_t)NBV * H * 2, n_rows, a, s);
+    if (nb <= NBV) return launch_split_v(k_gemv_nvfp4<NBV>, (size_t)NBV * H * 2, n_rows, a, s, false);
     VH_NVFP4_CASE(1)
     VH_NVFP4_CASE(2)
     VH_NVFP4_CASE(4)

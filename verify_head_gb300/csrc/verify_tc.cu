@@ -14,9 +14,9 @@
 // atom).  D lives in TMEM; two accumulator buffers of 256 columns let the
 // epilogue of tile i overlap the MMAs of tile i+1.  Scores never leave the
 // SM: the epilogue reads 32 columns at a time (thread = W row, register =
-// hidden row), packs (score, id) keys and reduces over the 32 W rows of its
-// warp with a 5-step transpose-reduce, so lane j ends up owning hidden row
-// g*32 + j.  Running maxima stay in registers across tiles; at the end the
+// hidden row); per column one redux.sync.max.f32 gives the warp maximum and
+// one ballot the lowest W row reaching it, and a select tree hands column j
+// to lane j.  Running maxima stay in registers across tiles; at the end the
 // four epilogue warps merge in shared memory and publish one atomicMax per
 // hidden row; the last CTA (ticket) decodes ids, runs the acceptance scan
 // and re-zeroes the workspace.
@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "vh_kernels.h"
+#include "vh_ptx.cuh"
 
 namespace vh {
 namespace tc {
@@ -47,7 +48,6 @@ constexpr int kEpiWarp0 = 2;
 constexpr int kStageA = kBlockM * kBlockK * 2;  // 16 KiB
 constexpr int kStageB = kMaxN * kBlockK * 2;    // 32 KiB
 constexpr int kTmemCols = 512;                  // two 256-column accumulators
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 struct alignas(8) Barriers {
     unsigned long long full[kStages];
@@ -76,67 +76,18 @@ struct TcArgs {
 };
 
 // ---------------------------------------------------------------------------
-// PTX wrappers.
+// tcgen05 / TMA wrappers (barriers and bulk copies: vh_ptx.cuh).
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
-                     smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on a barrier phase.  Returns false (and raises the error word)
-// if the phase does not complete within the time limit or an error is
-// already raised.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, unsigned int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            atomicOr(err, 1u);
-            return false;
-        }
-    }
-}
-
-// Bounded wait that ignores the error word (used to drain in-flight work
-// before the CTA releases its shared memory and TMEM).
-__device__ __forceinline__ void mbar_drain(unsigned long long* bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kTimeoutNs) return;
-}
+using ptx::globaltimer;
+using ptx::mbar_arrive;
+using ptx::mbar_arrive_expect_tx;
+using ptx::mbar_drain;
+using ptx::mbar_init;
+using ptx::mbar_try_wait;
+using ptx::mbar_wait;
+using ptx::policy_evict_first;
+using ptx::policy_evict_last;
+using ptx::smem_u32;
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, unsigned long long* bar, int x, int y,
                                             unsigned long long policy) {
@@ -145,18 +96,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<unsigned long long>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
-}
-
-__device__ __forceinline__ unsigned long long policy_evict_first() {
-    unsigned long long p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ unsigned long long policy_evict_last() {
-    unsigned long long p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -214,26 +153,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-    return a > b ? a : b;
+__device__ __forceinline__ float redux_max_f32(float x) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
 }
 
-// Transpose-reduce: v[j] is this lane's key for column j; afterwards lane j
-// holds the maximum over all 32 lanes of column j (returned).
-__device__ __forceinline__ unsigned long long transpose_max32(unsigned long long (&v)[32]) {
+// Column argmax over the warp's 32 W rows for 32 hidden columns at once.
+// v[j] is this lane's (W row's) score for column j.  For every column the
+// warp maximum comes from one redux and the lowest winning lane from one
+// ballot; a 5-level select tree then hands column `lane` to this lane:
+// returns its maximum and the ballot of lanes reaching it (0 = none valid).
+__device__ __forceinline__ void column_argmax32(const float (&v)[32], bool valid, float& m_out, uint32_t& b_out) {
     const int lane = threadIdx.x & 31;
+    float m[32];
+    uint32_t b[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float x = valid ? v[j] : -__int_as_float(0x7f800000);
+        m[j] = redux_max_f32(x);
+        b[j] = __ballot_sync(0xFFFFFFFFu, valid && x == m[j]);
+    }
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
+        const bool hi = (lane & s) != 0;
 #pragma unroll
         for (int i = 0; i < s; ++i) {
-            const unsigned long long send = upper ? v[i] : v[i + s];
-            const unsigned long long keep = upper ? v[i + s] : v[i];
-            const unsigned long long recv = __shfl_xor_sync(0xFFFFFFFFu, send, s);
-            v[i] = umax64(keep, recv);
+            m[i] = hi ? m[i + s] : m[i];
+            b[i] = hi ? b[i + s] : b[i];
         }
     }
-    return v[0];
+    m_out = m[0];
+    b_out = b[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -335,34 +286,45 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;  // TMEM lanes quarter*32 .. +31
         const int ngroups = (a.N + 31) / 32;
-        unsigned long long best[kMaxN / 32];
+        float best_v[kMaxN / 32];
+        uint32_t best_g[kMaxN / 32];
 #pragma unroll
-        for (int g = 0; g < kMaxN / 32; ++g) best[g] = 0ull;
+        for (int g = 0; g < kMaxN / 32; ++g) {
+            best_v[g] = -__int_as_float(0x7f800000);
+            best_g[g] = 0xFFFFFFFFu;  // none yet
+        }
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++local) {
             const uint32_t buf = local & 1u;
             if (!mbar_wait(&bars->tmem_full[buf], (local >> 1) & 1u, a.err)) break;
             tc_fence_after();
-            const int row = tile * kBlockM + quarter * 32 + lane;  // this thread's W row (global id)
-            const bool valid = row < a.V;
+            const uint32_t row0 = (uint32_t)(tile * kBlockM + quarter * 32);  // id of lane 0's W row
+            const bool valid = (int)(row0 + lane) < a.V;
 #pragma unroll
             for (int g = 0; g < kMaxN / 32; ++g) {
                 if (g < ngroups) {
                     float v[32];
                     tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 256u + g * 32u, v);
-                    unsigned long long key[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) key[j] = valid ? make_key(v[j], (uint32_t)row) : 0ull;
-                    best[g] = umax64(best[g], transpose_max32(key));
+                    if (g + 1 == ngroups) {  // accumulator fully read: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
+                    }
+                    float m;
+                    uint32_t bal;
+                    column_argmax32(v, valid, m, bal);
+                    // tiles arrive in increasing row order: strict '>' keeps the lower id on ties
+                    if (bal != 0u && (best_g[g] == 0xFFFFFFFFu || m > best_v[g])) {
+                        best_v[g] = m;
+                        best_g[g] = row0 + (uint32_t)(__ffs(bal) - 1);
+                    }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
         }
 #pragma unroll
         for (int g = 0; g < kMaxN / 32; ++g)
-            if (g < ngroups && best[g] != 0ull) atomicMax(&merge[g * 32 + lane], best[g]);
+            if (g < ngroups && best_g[g] != 0xFFFFFFFFu)
+                atomicMax(&merge[g * 32 + lane], make_key(best_v[g], best_g[g]));
     }
 
     // ---------------- CTA merge, publish, last-CTA decode ----------------
