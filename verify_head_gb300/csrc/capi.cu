@@ -11,7 +11,8 @@
 namespace {
 
 constexpr int kGemvRows = 8;   // hidden rows per CUDA-core launch
-constexpr int kTcRows = 256;   // hidden rows per tensor-core launch
+constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
+constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMaxDraftB = 256;
 constexpr int kMaxH = 65536;
 
@@ -114,11 +115,16 @@ vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const vh::Workspace w = make_ws(ws, B);
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
-    const int grp = gemv_group(H);
+    // one hidden row: CUDA-core streaming GEMV; more: tensor cores when H is a
+    // multiple of the 512-element raw stage, else CUDA cores
+    const bool tc = (B > 1 && H % 512 == 0);
+    const int grp = tc ? kTcFp4Rows : gemv_group(H);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
-        cudaError_t e = vh::launch_gemv_nvfp4(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w,
-                                              ids + b0, maxlogit + b0, s);
+        cudaError_t e = tc ? vh::launch_nvfp4_tc(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w,
+                                                 ids + b0, maxlogit + b0, s)
+                           : vh::launch_gemv_nvfp4(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc,
+                                                   w, ids + b0, maxlogit + b0, s);
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;

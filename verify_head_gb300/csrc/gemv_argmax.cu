@@ -448,6 +448,115 @@ static cudaError_t launch_ring_nvfp4(GemvArgs& a, cudaStream_t s) {
     return cudaErrorNotSupported;
 }
 
+
+// ---------------------------------------------------------------------------
+// Block-scaled 4-bit head, B = 1, H % 64 == 0, H <= 8192: direct streaming.
+// Each warp owns a contiguous run of rows and reads every code row with
+// 256-bit loads (one 64-element chunk = 32 code bytes + 4 scale bytes per
+// lane), two rows in flight.  The hidden row is held in registers as f16,
+// prescaled by 2^k so that its largest magnitude lies in [2^14, 2^15)
+// (exact for every element within 2^31 of the largest); weights decode with
+// cvt.rn.f16x2.e2m1x2 and accumulate in fp32 with fma.rn.f32.f16; each
+// 16-element block sum is multiplied by its E4M3 scale, the row by g*2^-k.
+
+template <int CPL>
+__global__ void __launch_bounds__(kThreads, (CPL >= 4 ? 1 : 2)) k_gemv_nvfp4_direct(const GemvArgs a) {
+    __shared__ float s_xmax[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = a.H, nch = H >> 6;
+    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
+    const uint8_t* __restrict__ Wq = static_cast<const uint8_t*>(a.W);
+
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long r0 = gw * a.rows_per_warp;
+    const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
+
+    pdl_launch_dependents();
+    for (long long r = r0; r < min(r1, r0 + 2); ++r)
+        for (int c = lane; c < nch; c += 32) prefetch_l2(Wq + (size_t)r * qrow + c * 32);
+    pdl_wait();
+
+    // power-of-two prescale from the largest |x| (identical in every CTA)
+    float m = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) s_xmax[warp] = m;
+    __syncthreads();
+    float xmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) xmax = fmaxf(xmax, s_xmax[w]);
+    const int k = xmax > 0.f ? min(127, 141 - (int)((__float_as_uint(xmax) >> 23) & 0xFF)) : 0;
+    const float up = ldexpf(1.f, k), out_scale = a.g * ldexpf(1.f, -k);
+
+    uint32_t xh[CPL][32];  // lane's chunks of x as f16x2 (element 2i in the low half)
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = lane + 32 * j;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            if (c < nch) {
+                const uint32_t pr = reinterpret_cast<const uint32_t*>(a.x)[c * 32 + t];
+                xh[j][t] = f32x2_to_h2(bf_lo(pr) * up, bf_hi(pr) * up);
+            } else {
+                xh[j][t] = 0u;
+            }
+        }
+    }
+
+    unsigned long long best = 0ull;
+    for (long long r = r0; r < r1; r += 2) {
+        const bool two = (r + 1 < r1);
+        U32x8 q0[CPL], q1[CPL];
+        uint32_t s0[CPL], s1[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                q0[j] = ld_stream32(Wq + (size_t)r * qrow + c * 32);
+                s0[j] = __ldg(reinterpret_cast<const uint32_t*>(a.scales + (size_t)r * srow) + c);
+                if (two) {
+                    q1[j] = ld_stream32(Wq + (size_t)(r + 1) * qrow + c * 32);
+                    s1[j] = __ldg(reinterpret_cast<const uint32_t*>(a.scales + (size_t)(r + 1) * srow) + c);
+                }
+            }
+        }
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                const float2 a01 = e4m3x2_to_f2(s0[j] & 0xFFFFu), a23 = e4m3x2_to_f2(s0[j] >> 16);
+                acc0 = fmaf(nvfp4_block16(q0[j].v[0], q0[j].v[1], &xh[j][0]), a01.x, acc0);
+                acc0 = fmaf(nvfp4_block16(q0[j].v[2], q0[j].v[3], &xh[j][8]), a01.y, acc0);
+                acc0 = fmaf(nvfp4_block16(q0[j].v[4], q0[j].v[5], &xh[j][16]), a23.x, acc0);
+                acc0 = fmaf(nvfp4_block16(q0[j].v[6], q0[j].v[7], &xh[j][24]), a23.y, acc0);
+                if (two) {
+                    const float2 b01 = e4m3x2_to_f2(s1[j] & 0xFFFFu), b23 = e4m3x2_to_f2(s1[j] >> 16);
+                    acc1 = fmaf(nvfp4_block16(q1[j].v[0], q1[j].v[1], &xh[j][0]), b01.x, acc1);
+                    acc1 = fmaf(nvfp4_block16(q1[j].v[2], q1[j].v[3], &xh[j][8]), b01.y, acc1);
+                    acc1 = fmaf(nvfp4_block16(q1[j].v[4], q1[j].v[5], &xh[j][16]), b23.x, acc1);
+                    acc1 = fmaf(nvfp4_block16(q1[j].v[6], q1[j].v[7], &xh[j][24]), b23.y, acc1);
+                }
+            }
+        }
+        {
+            const float sc = warp_sum(acc0) * out_scale;
+            const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
+            const unsigned long long kk = make_key(sc, gid);
+            best = kk > best ? kk : best;
+        }
+        if (two) {
+            const float sc = warp_sum(acc1) * out_scale;
+            const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1);
+            const unsigned long long kk = make_key(sc, gid);
+            best = kk > best ? kk : best;
+        }
+    }
+    unsigned long long b1[1] = {best};
+    finish_argmax<1>(b1, a);
+}
+
 // ---------------------------------------------------------------------------
 // Block-scaled 4-bit head on CUDA cores, any B <= 8.  A lane chunk is 32 code
 // bytes = 64 elements = 4 scale blocks.  Each 16-element block is summed
@@ -603,7 +712,12 @@ cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* W
     a.x = x; a.W = Wq; a.scales = scales; a.g = g; a.cand = cand;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit;
     a.err = ws.ticket + 1;
-    if (nb == 1 && H <= 8192 && H % 256 == 0) return launch_ring_nvfp4(a, s);  // scale rows of 16-byte multiples
+    if (nb == 1 && H <= 8192) {
+        const int cpl = (H / 64 + 31) / 32;
+        if (cpl <= 1) return launch_split_v(k_gemv_nvfp4_direct<1>, 0, n_rows, a, s, true);
+        if (cpl <= 2) return launch_split_v(k_gemv_nvfp4_direct<2>, 0, n_rows, a, s, true);
+        return launch_split_v(k_gemv_nvfp4_direct<4>, 0, n_rows, a, s, true);
+    }
 #define VH_NVFP4_CASE(NBV) \
     if (nb <= NBV) return launch_split_v(k_gemv_nvfp4<NBV>, (size_t)NBV * H * 2, n_rows, a, s, false);
     VH_NVFP4_CASE(1)
