@@ -337,6 +337,10 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"
         out.update(measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=(only == "verify")))
     if only in ("all", "sweep"):
         out["sweep"] = measure_sweep(torch, vh, synth, timer, peaks)
+    if only in ("all", "gather"):
+        out["gather"] = measure_gather(torch, vh, synth, timer, peaks)
+    if only in ("all", "chain"):
+        out["chain_graph"] = measure_chain_graph(torch, vh, synth, timer, peaks)
     if only in ("all", "nvfp4"):
         out["nvfp4"] = measure_nvfp4(torch, vh, synth, timer, peaks)
     return out
@@ -405,6 +409,55 @@ def measure_sweep(torch, vh, synth, timer, peaks):
                           "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
         del Wc
     return sweep
+
+
+def measure_gather(torch, vh, synth, timer, peaks):
+    """Dynamic candidate rows read in place: 32,768 fixed + 16,384 per-step
+    rows of the 248,320 x 2048 head, B = 1."""
+    dev = torch.device("cuda")
+    W = torch.from_numpy(synth.full_head(2, synth.V_FULL, 2048).view(np.int16)).to(dev)
+    rows = torch.from_numpy(synth.gather_row_ids(6, synth.V_FULL, step=0)).to(dev)
+    x = torch.from_numpy(synth.normal_bf16(2, synth.STREAM_HIDDEN, (1, 2048), 1.0).view(np.int16)).to(dev)
+    w1 = vh.workspace(1)
+    us = timer.time_calls(lambda: vh.mtp_draft_head_argmax_gather(x, W, rows, ws=w1), 20)
+    med = statistics.median(us)
+    n = rows.numel()
+    nbytes = n * 2048 * 2 + n * 4 + 4096
+    return {"workload": "32,768 fixed + 16,384 dynamic rows gathered from 248,320 x 2048 bf16, B=1",
+            "steps_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
+def measure_chain_graph(torch, vh, synth, timer, peaks):
+    """The 3-step draft chain (65,536 x 2048, B = 1) captured once as a CUDA
+    graph and replayed (L2 flushed before each replay)."""
+    dev = torch.device("cuda")
+    case = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
+    W = torch.from_numpy(case.W.view(np.int16)).to(dev)
+    cand = torch.from_numpy(case.cand_ids).to(dev)
+    xs = [torch.from_numpy(h.view(np.int16)).to(dev) for h in case.hidden]
+    ws = vh.workspace(1)
+    ids = [torch.empty(1, dtype=torch.int32, device=dev) for _ in range(3)]
+    mls = [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(3)]
+
+    def chain():
+        for i in range(3):
+            vh.mtp_draft_head_argmax(xs[i], W, cand, ids=ids[i], maxlogit=mls[i], ws=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    us = timer.time_calls(g.replay, 30)
+    med = statistics.median(us)
+    nbytes = 3 * (case.Vc * case.H * 2 + case.Vc * 4 + case.H * 2)
+    return {"workload": "3 draft steps of 65,536 x 2048 bf16, B=1, one graph replay", "us_per_chain": stats(us),
+            "draft_steps_per_s": round(3e6 / med, 1), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
 def measure_nvfp4(torch, vh, synth, timer, peaks):
@@ -499,7 +552,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
-    ap.add_argument("--workload", default="all", choices=["all", "draft", "verify", "sweep", "nvfp4"],
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "draft", "verify", "sweep", "nvfp4", "gather", "chain"],
                     help="all = the bench line; others run one measurement only (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -93,6 +93,31 @@ VH_API vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, c
                                 int Vc, int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Draft head over candidate rows gathered from the full head (dynamic
+ * candidate rows): no copy of the candidate table is made.
+ *
+ * "少读一张大表，草稿路径才真正快起来" reports upstream work (vLLM #59740) that
+ * scores 32K fixed plus 16K per-step dynamic candidate rows; the fixed rows
+ * can live in a separate table (mtp_draft_head_argmax), while a per-step set
+ * is best read in place.  For each hidden row b < B:
+ *     s[b,i]      = sum_h hidden[b,h] * W_full[row_ids[i],h]   (fp32 accumulation)
+ *     ids[b]      = row_ids[argmax_i s[b,i]]     (ties: the lowest row id)
+ *     maxlogit[b] = max_i s[b,i]
+ *
+ *  hidden    device, bf16 [B][H], 16-byte aligned
+ *  W_full    device, bf16 [V][H] row-major, 32-byte aligned
+ *  row_ids   device, int32 [n_ids], any order, repeats allowed; entries
+ *            outside [0, V) are ignored (never read).  At least one entry
+ *            must lie in [0, V), otherwise ids/maxlogit are unspecified.
+ *  B         1 <= B <= 256;  H: 16 <= H <= 65536, H % 16 == 0
+ *  n_ids     >= 1;  V >= 1
+ *  ids, maxlogit, ws: as for mtp_draft_head_argmax
+ */
+VH_API vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_full, const int32_t* row_ids, int B,
+                                              int H, int n_ids, int V, int32_t* ids, float* maxlogit, void* ws,
+                                              size_t ws_bytes, void* stream);
+
+/*
  * Restricted-vocabulary draft head, block-scaled 4-bit weights (NVFP4).
  *
  * Weight (c, h) = e2m1(code) * e4m3(scales[c][h/16]) * tensor_scale, where

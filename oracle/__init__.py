@@ -16,6 +16,8 @@ Parity status per function (what pins it; see tests/test_oracle_pins.py):
                       float8_e4m3fn), fp64 brute force with exact rational
                       decoding, nibble/scale-order fixtures, equality with
                       draft_argmax on an exactly representable head
+  draft_argmax_gather exact-integer brute force with unsorted and repeated
+                      ids, equality with draft_argmax on the sorted set
   verify_greedy       exact-integer brute force, hand-built acceptance
                       fixtures (tests/golden/accept_cases.txt), equality with
                       draft_argmax over the identity candidate set
@@ -74,6 +76,8 @@ def lib():
         L.vh_oracle_draft_argmax.restype = i32
         L.vh_oracle_draft_argmax_nvfp4.argtypes = [vp, vp, vp, f32, vp, i64, i64, i64, vp, vp, vp, i32]
         L.vh_oracle_draft_argmax_nvfp4.restype = i32
+        L.vh_oracle_draft_argmax_gather.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, i32]
+        L.vh_oracle_draft_argmax_gather.restype = i32
         L.vh_oracle_accept_len.argtypes = [vp, vp, i64]
         L.vh_oracle_accept_len.restype = ctypes.c_int32
         L.vh_oracle_verify_greedy.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i64, vp, vp, vp, vp, i32]
@@ -142,6 +146,24 @@ def draft_argmax_nvfp4(x, q, s, g, cand_ids, nthreads: int | None = None):
                                             sec.ctypes.data, nthreads or threads())
     if rc != 0:
         raise ValueError(f"oracle draft_argmax_nvfp4 failed ({rc})")
+    return ids, ml, sec
+
+
+def draft_argmax_gather(x, W_full, row_ids, nthreads: int | None = None):
+    """x uint16 [B,H], W_full uint16 [V,H], row_ids int32 [n] -> (ids, maxlogit, second)."""
+    x, px = _c(x, np.uint16)
+    W, pW = _c(W_full, np.uint16)
+    r, pr = _c(row_ids, np.int32)
+    B, H = x.shape
+    V = W.shape[0]
+    assert W.shape[1] == H
+    ids = np.empty(B, np.int32)
+    ml = np.empty(B, np.float32)
+    sec = np.empty(B, np.float32)
+    rc = lib().vh_oracle_draft_argmax_gather(px, pW, pr, B, H, r.size, V, ids.ctypes.data, ml.ctypes.data,
+                                             sec.ctypes.data, nthreads or threads())
+    if rc != 0:
+        raise ValueError(f"oracle draft_argmax_gather failed ({rc})")
     return ids, ml, sec
 
 

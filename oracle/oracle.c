@@ -99,6 +99,7 @@ float vh_oracle_dot_nvfp4(const uint16_t* x, const uint8_t* q, const uint8_t* s,
 typedef struct {
     const uint16_t* x;
     const uint16_t* W;  /* bf16 head, or NULL for the 4-bit head */
+    const int32_t* rows; /* score W row rows[c] for entry c (NULL: row c) */
     const uint8_t* q;
     const uint8_t* s;
     float g;
@@ -111,15 +112,15 @@ static void* score_main(void* p) {
     score_job* j = (score_job*)p;
     for (int64_t c = j->lo; c < j->hi; ++c) {
         if (j->W)
-            j->out[c] = vh_oracle_dot_bf16(j->x, j->W + c * j->H, j->H);
+            j->out[c] = vh_oracle_dot_bf16(j->x, j->W + (j->rows ? (int64_t)j->rows[c] : c) * j->H, j->H);
         else
             j->out[c] = vh_oracle_dot_nvfp4(j->x, j->q + c * (j->H / 2), j->s + c * (j->H / 16), j->g, j->H);
     }
     return NULL;
 }
 
-static void all_scores(const uint16_t* x, const uint16_t* W, const uint8_t* q, const uint8_t* s, float g,
-                       int64_t n, int64_t H, float* out, int nthreads) {
+static void all_scores_rows(const uint16_t* x, const uint16_t* W, const int32_t* rows, const uint8_t* q,
+                            const uint8_t* s, float g, int64_t n, int64_t H, float* out, int nthreads) {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if (n < 64) nthreads = 1;
@@ -127,7 +128,7 @@ static void all_scores(const uint16_t* x, const uint16_t* W, const uint8_t* q, c
     pthread_t th[256];
     int started = 0;
     for (int t = 0; t < nthreads; ++t) {
-        score_job j = {x, W, q, s, g, H, out, n * t / nthreads, n * (t + 1) / nthreads};
+        score_job j = {x, W, rows, q, s, g, H, out, n * t / nthreads, n * (t + 1) / nthreads};
         jobs[t] = j;
     }
     for (int t = 0; t + 1 < nthreads; ++t) {
@@ -136,6 +137,11 @@ static void all_scores(const uint16_t* x, const uint16_t* W, const uint8_t* q, c
     }
     for (int t = started; t < nthreads; ++t) score_main(&jobs[t]);
     for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+}
+
+static void all_scores(const uint16_t* x, const uint16_t* W, const uint8_t* q, const uint8_t* s, float g, int64_t n,
+                       int64_t H, float* out, int nthreads) {
+    all_scores_rows(x, W, NULL, q, s, g, n, H, out, nthreads);
 }
 
 /* Sequential scan: first index of the maximum (strict >), NaN as -inf,
@@ -195,6 +201,46 @@ int vh_oracle_draft_argmax_nvfp4(const uint16_t* x, const uint8_t* q, const uint
         if (second) second[b] = sv;
     }
     free(sc);
+    return 0;
+}
+
+/* Draft head over rows gathered from the full head (dynamic candidate rows):
+ * entry i scores W row row_ids[i] (entries outside [0, V) are ignored); the
+ * largest score wins and equal scores go to the lowest row id, whatever the
+ * order of the list.  second[b] = best score among entries with another id.
+ * Returns -3 if no entry is in range. */
+int vh_oracle_draft_argmax_gather(const uint16_t* x, const uint16_t* W, const int32_t* row_ids, int64_t B, int64_t H,
+                                  int64_t n, int64_t V, int32_t* ids, float* maxlogit, float* second, int nthreads) {
+    if (B < 1 || H < 1 || n < 1 || V < 1) return -1;
+    float* sc = (float*)malloc((size_t)n * sizeof(float));
+    int32_t* rows = (int32_t*)malloc((size_t)n * sizeof(int32_t));
+    if (!sc || !rows) { free(sc); free(rows); return -2; }
+    for (int64_t i = 0; i < n; ++i) rows[i] = (row_ids[i] >= 0 && row_ids[i] < V) ? row_ids[i] : 0;
+    for (int64_t b = 0; b < B; ++b) {
+        all_scores_rows(x + b * H, W, rows, NULL, NULL, 0.0f, n, H, sc, nthreads);
+        int64_t best = -1;
+        float bv = -INFINITY;
+        for (int64_t i = 0; i < n; ++i) {
+            if (row_ids[i] < 0 || row_ids[i] >= V) continue;
+            float v = isnan(sc[i]) ? -INFINITY : sc[i];
+            if (best < 0 || v > bv || (v == bv && row_ids[i] < row_ids[best])) {
+                best = i;
+                bv = v;
+            }
+        }
+        if (best < 0) { free(sc); free(rows); return -3; }
+        float sv = -INFINITY;
+        for (int64_t i = 0; i < n; ++i) {
+            if (row_ids[i] < 0 || row_ids[i] >= V || row_ids[i] == row_ids[best]) continue;
+            float v = isnan(sc[i]) ? -INFINITY : sc[i];
+            if (v > sv) sv = v;
+        }
+        ids[b] = row_ids[best];
+        maxlogit[b] = bv + 0.0f;
+        if (second) second[b] = sv;
+    }
+    free(sc);
+    free(rows);
     return 0;
 }
 

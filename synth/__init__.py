@@ -34,6 +34,7 @@ STREAM_HIDDEN = 3
 STREAM_VHIDDEN = 4
 STREAM_CORRUPT = 5
 STREAM_W4 = 6
+STREAM_DYN = 7
 
 _lib = None
 
@@ -281,3 +282,13 @@ def nvfp4_case(Vc: int = 65_536, H: int = 4096, B: int = 1, steps: int = 3, seed
     q, s, g = nvfp4_quantize(w)
     return Nvfp4Case(f"nvfp4-{Vc}x{H}-B{B}", draft_hidden(seed, steps, B, H), q, s, g, cand,
                      {"V": V, "seed": seed})
+
+
+def gather_row_ids(seed: int = 6, V: int = V_FULL, n_fixed: int = 32_768, n_dynamic: int = 16_384,
+                   step: int = 0) -> np.ndarray:
+    """Candidate rows read in place from the full head: a fixed sorted set of
+    n_fixed ids followed by a per-step sorted set of n_dynamic ids (the two
+    may overlap), as int32 [n_fixed + n_dynamic]."""
+    fixed = sorted_subset(seed, STREAM_CAND, V, n_fixed)
+    dyn = sorted_subset(seed * 1000 + step, STREAM_DYN, V, n_dynamic)
+    return np.concatenate([fixed, dyn]).astype(np.int32)

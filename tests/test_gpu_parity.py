@@ -154,6 +154,63 @@ def test_restricted_equals_full_when_top1_is_candidate(vh, syn):
 
 
 # ----------------------------------------------------------------------------
+# gathered (dynamic) candidate rows, read in place from the full head
+
+
+def run_gather(vh, x, W_full, rows):
+    import torch
+    ids, ml = vh.mtp_draft_head_argmax_gather(to_torch_bf16(x), to_torch_bf16(W_full), to_torch(rows))
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), ml.cpu().numpy()
+
+
+def check_gather(vh, orc, x, W_full, rows):
+    g_ids, g_ml = run_gather(vh, x, W_full, rows)
+    o_ids, o_ml, o_sec = orc.draft_argmax_gather(x, W_full, rows)
+    valid = set(int(r) for r in rows if 0 <= r < W_full.shape[0])
+
+    def score_of(r, gid):
+        assert int(gid) in valid, "GPU returned an id outside the gathered set"
+        return orc.dot_bf16(x[r], W_full[gid])
+
+    check_ids(g_ids, g_ml, o_ids, o_ml, o_sec, score_of, TOL_BF16)
+
+
+@pytest.mark.parametrize("V,H,B,n", [(5000, 256, 1, 1), (5000, 256, 2, 777), (20_000, 2048, 1, 9000),
+                                     (3000, 4096, 3, 2999), (7000, 6144, 1, 500)])
+def test_gather_shapes(vh, orc, syn, V, H, B, n):
+    W = syn.normal_bf16(V + 1, 1, (V, H), 0.02)
+    x = syn.normal_bf16(B + 2, 3, (B, H), 1.0)
+    rng = np.random.default_rng(V + n)
+    rows = rng.integers(-5, V + 5, size=n).astype(np.int32)  # unsorted, repeats, a few out of range
+    rows[0] = 17
+    check_gather(vh, orc, x, W, rows)
+
+
+def test_gather_fixed_plus_dynamic_full_head(vh, orc, syn):
+    """32,768 fixed + 16,384 per-step dynamic candidate rows read in place
+    from the 248,320 x 2048 head, B = 1, three steps."""
+    W_full = syn.full_head(2, syn.V_FULL, 2048)
+    for step in range(3):
+        rows = syn.gather_row_ids(6, syn.V_FULL, step=step)
+        x = syn.normal_bf16(2, syn.STREAM_HIDDEN, (1, 2048), 1.0, offset=step * 2048)
+        check_gather(vh, orc, x, W_full, rows)
+
+
+def test_gather_matches_candidate_table_kernel(vh, syn):
+    """Same candidate set as a sorted copied table: same ids and maxima."""
+    V, H = 30_000, 1024
+    W = syn.normal_bf16(5, 1, (V, H), 0.02)
+    cand = syn.sorted_subset(5, 2, V, 6000)
+    x = syn.normal_bf16(6, 3, (4, H), 1.0)
+    perm = np.random.default_rng(0).permutation(cand).astype(np.int32)
+    g_ids, g_ml = run_gather(vh, x, W, perm)
+    t_ids, t_ml = run_draft(vh, x, np.ascontiguousarray(W[cand]), cand)
+    np.testing.assert_array_equal(g_ids, t_ids)
+    np.testing.assert_array_equal(g_ml, t_ml)
+
+
+# ----------------------------------------------------------------------------
 # 4-bit draft head
 
 

@@ -398,3 +398,36 @@ def test_nvfp4_equals_bf16_on_representable_head(oracle_mod):
     b = oracle_mod.draft_argmax(xb, Wb, cand)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+# --------------------------------------------------------------------------
+# Gathered candidate rows (ids in any order, repeats, out-of-range entries).
+
+@pytest.mark.parametrize("seed", range(8))
+def test_gather_exact_integers(oracle_mod, seed):
+    rng = np.random.default_rng(5000 + seed)
+    V, H, B = int(rng.integers(2, 40)), int(rng.integers(1, 12)), int(rng.integers(1, 4))
+    Wi = rng.integers(-2, 3, size=(V, H))
+    xi = rng.integers(-2, 3, size=(B, H))
+    n = int(rng.integers(1, 60))
+    rows = rng.integers(-3, V + 3, size=n).astype(np.int32)  # includes out-of-range entries
+    rows[0] = int(rng.integers(0, V))                        # at least one valid entry
+    ids, ml, _ = oracle_mod.draft_argmax_gather(bf16_bits(xi), bf16_bits(Wi), rows)
+    for b in range(B):
+        valid = [int(r) for r in rows if 0 <= r < V]
+        s = {r: sum(int(xi[b, h]) * int(Wi[r, h]) for h in range(H)) for r in valid}
+        best = max(s.values())
+        assert ml[b] == best
+        assert ids[b] == min(r for r, v in s.items() if v == best)  # lowest id on ties, any list order
+
+
+def test_gather_equals_sorted_candidate_table(oracle_mod, synth_mod):
+    _, verify, W_full = synth_mod.tiny_case()
+    rng = np.random.default_rng(3)
+    rows = rng.integers(0, W_full.shape[0], size=700).astype(np.int32)
+    uniq = np.unique(rows).astype(np.int32)
+    x = synth_mod.normal_bf16(8, synth_mod.STREAM_HIDDEN, (3, W_full.shape[1]), 1.0)
+    a = oracle_mod.draft_argmax_gather(x, W_full, rows)
+    b = oracle_mod.draft_argmax(x, np.ascontiguousarray(W_full[uniq]), uniq)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])

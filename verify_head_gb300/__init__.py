@@ -33,7 +33,7 @@ VH_PATH_TENSOR = 2
 EXPORTS = (
     "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
-    "mtp_draft_head_argmax_static_ws",
+    "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather",
 )
 
 
@@ -71,6 +71,8 @@ def lib():
         L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
         L.spec_verify_greedy.restype = i32
         L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.mtp_draft_head_argmax_gather.restype = i32
+        L.mtp_draft_head_argmax_gather.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         L.mtp_draft_head_argmax_static_ws.restype = i32
         L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.spec_verify_greedy_path.restype = i32
@@ -142,6 +144,27 @@ def mtp_draft_head_argmax(hidden, W_cand, cand_ids, ids=None, maxlogit=None, ws=
     st = lib().mtp_draft_head_argmax(_ptr(hidden), _ptr(W_cand), _ptr(cand_ids), B, H, Vc, _ptr(ids), _ptr(maxlogit),
                                      _ptr(ws), ws.numel(), _stream_ptr(stream))
     _check(st, "mtp_draft_head_argmax")
+    return ids, maxlogit
+
+
+def mtp_draft_head_argmax_gather(hidden, W_full, row_ids, ids=None, maxlogit=None, ws=None, stream=None):
+    """hidden [B,H] bf16, W_full [V,H] bf16, row_ids [n] int32 (rows of W_full to score, any order)
+    -> (ids [B] int32 = winning row ids, maxlogit [B] fp32)."""
+    torch = _torch()
+    _require_cuda(hidden, W_full, row_ids)
+    B, H = hidden.shape
+    V = W_full.shape[0]
+    if W_full.shape[1] != H or hidden.element_size() != 2 or W_full.element_size() != 2:
+        raise ValueError("shape/dtype mismatch")
+    if ids is None:
+        ids = torch.empty(B, dtype=torch.int32, device=hidden.device)
+    if maxlogit is None:
+        maxlogit = torch.empty(B, dtype=torch.float32, device=hidden.device)
+    if ws is None:
+        ws = workspace(B, hidden.device)
+    st = lib().mtp_draft_head_argmax_gather(_ptr(hidden), _ptr(W_full), _ptr(row_ids), B, H, row_ids.numel(), V,
+                                            _ptr(ids), _ptr(maxlogit), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(st, "mtp_draft_head_argmax_gather")
     return ids, maxlogit
 
 

@@ -100,6 +100,30 @@ vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const in
     return VH_OK;
 }
 
+vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_full, const int32_t* row_ids, int B, int H,
+                                       int n_ids, int V, int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes,
+                                       void* stream) {
+    if (!hidden || !W_full || !row_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
+    if (B < 1 || B > kMaxDraftB || H < 16 || H > kMaxH || H % 16 != 0 || n_ids < 1 || V < 1) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(W_full, 32) || !aligned(row_ids, 4) || !aligned(ids, 4) ||
+        !aligned(maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    if (ws_bytes < vh_workspace_bytes(B)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, B);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const int grp = gemv_group(H);
+    for (int b0 = 0; b0 < B; b0 += grp) {
+        const int nb = std::min(grp, B - b0);
+        cudaError_t e = vh::launch_gemv_bf16(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_full), row_ids,
+                                             n_ids, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s, V);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
 vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
                                       float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
                                       int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {

@@ -31,6 +31,8 @@ struct GemvArgs {
     const uint8_t* scales;  // [n_rows][H/16] E4M3 (4-bit head only)
     float g;                // tensor scale (4-bit head only)
     const int32_t* cand;    // [n_rows] or nullptr
+    int gather;             // 1: row r of the scan is W row cand[r] (rows outside [0, V) are skipped)
+    int V;                  // rows of W when gathering
     int nb;
     int H;
     int n_rows;
@@ -151,9 +153,16 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
     const long long r0 = gw * a.rows_per_warp;
     const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
 
+    // physical W row of scan position r (the identity unless gathering)
+    auto wrow = [&](long long r) -> long long { return a.gather ? (long long)__ldg(a.cand + r) : r; };
+    auto in_range = [&](long long pr) -> bool { return !a.gather || (pr >= 0 && pr < a.V); };
+
     pdl_launch_dependents();
-    for (long long r = r0; r < min(r1, r0 + RPI); ++r)
-        for (int c = lane; c < min(nch, 128); c += 32) prefetch_l2(W + (size_t)r * H + c * 16);
+    for (long long r = r0; r < min(r1, r0 + RPI); ++r) {
+        const long long pr = wrow(r);
+        if (in_range(pr))
+            for (int c = lane; c < min(nch, 128); c += 32) prefetch_l2(W + (size_t)pr * H + c * 16);
+    }
     pdl_wait();
 
     {
@@ -172,9 +181,12 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
     for (int b = 0; b < NB; ++b) best[b] = 0ull;
 
     for (long long r = r0; r < r1; r += RPI) {
-        const bool two = RPI > 1 && (r + 1 < r1);
-        const uint16_t* w0p = W + (size_t)r * H;
-        const uint16_t* w1p = w0p + H;
+        const long long pr0 = wrow(r);
+        const long long pr1 = (RPI > 1 && r + 1 < r1) ? wrow(r + 1) : 0;
+        const bool ok0 = in_range(pr0);
+        const bool two = RPI > 1 && (r + 1 < r1) && in_range(pr1);
+        const uint16_t* w0p = W + (size_t)(ok0 ? pr0 : 0) * H;
+        const uint16_t* w1p = W + (size_t)(two ? pr1 : 0) * H;
         float p0[NB][2], p1[NB][2];
 #pragma unroll
         for (int b = 0; b < NB; ++b) p0[b][0] = p0[b][1] = p1[b][0] = p1[b][1] = 0.f;
@@ -184,14 +196,14 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
             for (int i = 0; i < 4; ++i) {
                 const int c = seg + lane + 32 * i;
                 if (c < nch) {
-                    w0[i] = ld_stream32(w0p + c * 16);
+                    if (ok0) w0[i] = ld_stream32(w0p + c * 16);
                     if (two) w1[RPI > 1 ? i : 0] = ld_stream32(w1p + c * 16);
                 }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int c = seg + lane + 32 * i;
-                if (c < nch) {
+                if (c < nch && ok0) {
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
                         const U32x8 xv = ld_x32(xs + (size_t)b * H + c * 16);
@@ -206,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const float s0 = warp_sum(p0[b][0] + p0[b][1]);
-            const unsigned long long k0 = make_key(s0, g0);
+            const unsigned long long k0 = ok0 ? make_key(s0, g0) : 0ull;
             best[b] = k0 > best[b] ? k0 : best[b];
             if (two) {
                 const float s1 = warp_sum(p1[b][0] + p1[b][1]);
@@ -690,9 +702,12 @@ static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a
 }
 
 cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
-                             Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+                             Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                             int gather_V) {
     GemvArgs a{};
     a.x = x; a.W = W; a.scales = nullptr; a.g = 1.f; a.cand = cand;
+    a.gather = gather_V > 0 ? 1 : 0;
+    a.V = gather_V;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit; a.tail = tail;
     a.err = ws.ticket + 1;
     if (nb == 1) return launch_split_v(k_gemv_bf16<1, 1>, (size_t)H * 2, n_rows, a, s, true);

@@ -19,9 +19,12 @@ struct AcceptTail {
 };
 
 // bf16 streaming GEMV + argmax over rows [0, n_rows) of W for nb <= 8 hidden
-// rows.  gid of row r is cand[r] (cand != nullptr) or r.
+// rows.  gid of row r is cand[r] (cand != nullptr) or r.  With gather_V > 0
+// the scan reads W row cand[r] of a [gather_V][H] head instead of row r (ids
+// outside [0, gather_V) are skipped).
 cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
-                             Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+                             Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                             int gather_V = 0);
 
 // Block-scaled 4-bit (E2M1 codes, E4M3 block scales, fp32 tensor scale)
 // GEMV + argmax on CUDA cores, nb <= 8.
