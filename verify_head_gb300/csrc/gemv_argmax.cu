@@ -142,6 +142,10 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
+// Rows (per warp) whose lines are prefetched into L2 ahead of the row being
+// loaded: more bytes in flight per SM without more registers.
+constexpr int kPrefetchRows = 1;
+
 template <int NB, int RPI>
 __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const GemvArgs a) {
     extern __shared__ __align__(16) uint16_t xs[];  // [NB][H]
@@ -180,9 +184,23 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
 #pragma unroll
     for (int b = 0; b < NB; ++b) best[b] = 0ull;
 
+    int idx_cache = 0;  // gathering: row ids of the next 32 scan positions, one per lane
     for (long long r = r0; r < r1; r += RPI) {
-        const long long pr0 = wrow(r);
-        const long long pr1 = (RPI > 1 && r + 1 < r1) ? wrow(r + 1) : 0;
+        if (a.gather && ((r - r0) & 31) == 0) {
+            const long long rr = r + lane;
+            idx_cache = rr < r1 ? __ldg(a.cand + rr) : -1;
+        }
+        if (kPrefetchRows > 0 && !a.gather) {  // keep rows ahead of the loads in flight to L2
+            const long long rp = r + kPrefetchRows * RPI;
+            for (int rr = 0; rr < RPI; ++rr)
+                if (rp + rr < r1)
+                    for (int c = lane * 8; c < nch; c += 256) prefetch_l2(W + (size_t)(rp + rr) * H + c * 16);
+        }
+        const long long pr0 = a.gather ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r - r0) & 31)) : r;
+        const long long pr1 =
+            (RPI > 1 && r + 1 < r1)
+                ? (a.gather ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r + 1 - r0) & 31)) : r + 1)
+                : 0;
         const bool ok0 = in_range(pr0);
         const bool two = RPI > 1 && (r + 1 < r1) && in_range(pr1);
         const uint16_t* w0p = W + (size_t)(ok0 ? pr0 : 0) * H;
@@ -213,8 +231,9 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
                 }
             }
         }
-        const uint32_t g0 = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
-        const uint32_t g1 = two ? (a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1)) : 0u;
+        const uint32_t g0 = a.gather ? (uint32_t)pr0 : (a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r);
+        const uint32_t g1 =
+            two ? (a.gather ? (uint32_t)pr1 : (a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1))) : 0u;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const float s0 = warp_sum(p0[b][0] + p0[b][1]);
