@@ -363,6 +363,261 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant for 129..256 hidden rows (tcgen05 cta_group::2).
+//
+// Two CTAs of a cluster share each MMA: M = 256 W rows (128 from each CTA's
+// shared memory), N = 256 hidden rows (128 from each CTA), K = 16.  Each CTA
+// therefore stages only half of the hidden tile (16 KiB per K-stage instead
+// of 32), which halves the shared-memory traffic per SM and lets the ring
+// hold 6 stages of 32 KiB.  The leader CTA (rank 0) issues the MMAs; both
+// CTAs' TMA loads complete on the leader's barrier, and the MMA completion
+// is multicast to both CTAs' barriers.  Each CTA's TMEM receives the
+// accumulator rows of its own 128 W rows, so the epilogue is unchanged.
+
+constexpr int kStages2 = 6;
+constexpr int kStageA2 = kBlockM * kBlockK * 2;  // 16 KiB: this CTA's 128 W rows
+constexpr int kStageB2 = 128 * kBlockK * 2;      // 16 KiB: this CTA's 128 hidden rows
+constexpr int kPairM = 2 * kBlockM;              // W rows per pair tile
+
+struct alignas(8) Barriers2 {
+    unsigned long long full[kStages2];   // leader only: both CTAs' loads land here
+    unsigned long long empty[kStages2];  // both CTAs: the MMA multicasts its completion
+    unsigned long long tmem_full[2];     // both CTAs
+    unsigned long long tmem_empty[2];    // leader only: 4 epilogue warps x 2 CTAs
+    unsigned long long mma_done;
+    unsigned int tmem_base;
+    unsigned int pad;
+};
+
+constexpr size_t kSmem2 = 1024 + (size_t)kStages2 * (kStageA2 + kStageB2) + sizeof(Barriers2) + kMaxN * 8 + 64;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory, completing on a barrier that may
+// live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x, int y,
+                                                 unsigned long long policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, unsigned long long adesc, unsigned long long bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at this offset in both CTAs once all prior MMAs are done.
+__device__ __forceinline__ void mma_commit_pair(unsigned long long* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((unsigned short)3)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    k_verify_tc2(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x, const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_a = smem;                                   // kStages2 x 16 KiB (this CTA's W rows)
+    uint8_t* stage_b = smem + (size_t)kStages2 * kStageA2;     // kStages2 x 16 KiB (this CTA's hidden rows)
+    Barriers2* bars = reinterpret_cast<Barriers2*>(stage_b + (size_t)kStages2 * kStageB2);
+    unsigned long long* merge = reinterpret_cast<unsigned long long*>(bars + 1);  // [kMaxN]
+    __shared__ unsigned int s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int n_ptiles = (a.V + kPairM - 1) / kPairM;
+    const int k_stages = a.H / kBlockK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->tmem_full[b], 1);
+            mbar_init(&bars->tmem_empty[b], 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(&bars->mma_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < kMaxN; i += blockDim.x) merge[i] = 0ull;
+    if (warp == 1) {  // one warp in each CTA of the pair allocates the paired TMEM
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars->tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0) {
+            const unsigned long long pol_w = policy_evict_first();
+            const unsigned long long pol_x = policy_evict_last();
+            uint32_t it = 0;
+            bool ok = true;
+            for (int pt = pair; pt < n_ptiles && ok; pt += n_pairs) {
+                for (int ks = 0; ks < k_stages; ++ks, ++it) {
+                    const int s = it % kStages2;
+                    if (!mbar_wait(&bars->empty[s], ((it / kStages2) & 1u) ^ 1u, a.err)) { ok = false; break; }
+                    const uint32_t full_leader = map_to_rank(smem_u32(&bars->full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&bars->full[s], 2u * (uint32_t)(kStageA2 + kStageB2));
+                    tma_load_2d_pair(stage_a + (size_t)s * kStageA2, &map_w, full_leader, ks * kBlockK,
+                                     pt * kPairM + (int)rank * kBlockM, pol_w);
+                    tma_load_2d_pair(stage_b + (size_t)s * kStageB2, &map_x, full_leader, ks * kBlockK,
+                                     (int)rank * 128, pol_x);
+                }
+            }
+            if (leader) {  // drain: the leader's barriers see both CTAs' loads
+                const uint32_t issued = it;
+                for (uint32_t j = (issued > (uint32_t)kStages2 ? issued - kStages2 : 0); j < issued; ++j)
+                    mbar_drain(&bars->full[j % kStages2], (j / kStages2) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader CTA only) ----------------
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16(kPairM, 256);
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int pt = pair; pt < n_ptiles && ok; pt += n_pairs, ++local) {
+                const uint32_t buf = local & 1u;
+                if (!mbar_wait(&bars->tmem_empty[buf], ((local >> 1) & 1u) ^ 1u, a.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * 256u;
+                for (int ks = 0; ks < k_stages; ++ks, ++it) {
+                    const int s = it % kStages2;
+                    if (!mbar_wait(&bars->full[s], (it / kStages2) & 1u, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(stage_a + (size_t)s * kStageA2);
+                    const uint32_t sb = smem_u32(stage_b + (size_t)s * kStageB2);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        mma_bf16_pair(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
+                                      (ks > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_pair(&bars->empty[s]);
+                }
+                if (ok) mma_commit_pair(&bars->tmem_full[buf]);
+            }
+            mma_commit_pair(&bars->mma_done);
+            mbar_drain(&bars->mma_done, 0u);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+        const int quarter = warp & 3;
+        float best_v[kMaxN / 32];
+        uint32_t best_g[kMaxN / 32];
+#pragma unroll
+        for (int g = 0; g < kMaxN / 32; ++g) {
+            best_v[g] = -__int_as_float(0x7f800000);
+            best_g[g] = 0xFFFFFFFFu;
+        }
+        const uint32_t empty_leader0 = map_to_rank(smem_u32(&bars->tmem_empty[0]), 0);
+        const uint32_t empty_leader1 = map_to_rank(smem_u32(&bars->tmem_empty[1]), 0);
+        uint32_t local = 0;
+        for (int pt = pair; pt < n_ptiles; pt += n_pairs, ++local) {
+            const uint32_t buf = local & 1u;
+            if (!mbar_wait(&bars->tmem_full[buf], (local >> 1) & 1u, a.err)) break;
+            tc_fence_after();
+            const uint32_t row0 = (uint32_t)(pt * kPairM + (int)rank * kBlockM + quarter * 32);
+            const bool valid = (int)(row0 + lane) < a.V;
+#pragma unroll
+            for (int g = 0; g < kMaxN / 32; ++g) {
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 256u + g * 32u, v);
+                if (g + 1 == kMaxN / 32) {  // accumulator fully read: release it to the leader's MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(buf ? empty_leader1 : empty_leader0);
+                }
+                float m;
+                uint32_t bal;
+                column_argmax32(v, valid, m, bal);
+                if (bal != 0u && (best_g[g] == 0xFFFFFFFFu || m > best_v[g])) {
+                    best_v[g] = m;
+                    best_g[g] = row0 + (uint32_t)(__ffs(bal) - 1);
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxN / 32; ++g)
+            if (best_g[g] != 0xFFFFFFFFu) atomicMax(&merge[g * 32 + lane], make_key(best_v[g], best_g[g]));
+    }
+
+    // ---------------- pair teardown, publish, last-CTA decode ----------------
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal or read it
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x)
+        if (merge[r] != 0ull) atomicMax(a.ws.keys + r, merge[r]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+        const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
+        a.next_ids[r] = (int32_t)key_gid(k);
+        if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
+    }
+    if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
+    if (a.tail.draft != nullptr) {
+        __threadfence();
+        __syncthreads();
+        const int k = a.tail.k;
+        for (int b = threadIdx.x; b < a.tail.B; b += blockDim.x) {
+            const volatile int32_t* nid = a.tail.next_ids + (size_t)b * (k + 1);
+            const int32_t* d = a.tail.draft + (size_t)b * k;
+            int acc = 0;
+            while (acc < k && nid[acc] == d[acc]) ++acc;
+            a.tail.accept_len[b] = acc;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps through the driver entry point (no libcuda link).
 
@@ -394,12 +649,55 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int H, int box_
     return r == CUDA_SUCCESS;
 }
 
+
+// CTA-pair launch (R in 129..256): clusters of 2, grid = 2 x the resident clusters.
+static cudaError_t launch_verify_tc2(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
+                                     int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    alignas(64) CUtensorMap map_w, map_x;
+    if (!make_map(&map_w, W, V, H, kBlockM) || !make_map(&map_x, X, R, H, 128)) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(k_verify_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem2);
+    if (e != cudaSuccess) return e;
+    TcArgs a{};
+    a.R = R;
+    a.N = 256;
+    a.H = H;
+    a.V = V;
+    a.n_tiles = (V + kPairM - 1) / kPairM;
+    a.ws = ws;
+    a.err = ws.ticket + 1;
+    a.next_ids = next_ids;
+    a.maxlogit = maxlogit;
+    a.tail = tail;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreadsTc);
+    cfg.dynamicSmemBytes = kSmem2;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(sm_count() / 2, a.n_tiles)));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k_verify_tc2, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(clusters, a.n_tiles)));
+    return cudaLaunchKernelEx(&cfg, k_verify_tc2, map_w, map_x, a);
+}
 }  // namespace tc
 
 cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
                              int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
     using namespace tc;
     if (R < 1 || R > kMaxN || H < kBlockK || H % kBlockK != 0 || V < 1) return cudaErrorNotSupported;
+    if (R > 128) {
+        cudaError_t e = launch_verify_tc2(X, R, H, W, V, ws, next_ids, maxlogit, tail, s);
+        if (e != cudaErrorNotSupported) return e;  // otherwise fall through to the single-CTA kernel
+    }
     const int N = (R + 15) / 16 * 16;
     alignas(64) CUtensorMap map_w, map_x;
     if (!make_map(&map_w, W, V, H, kBlockM) || !make_map(&map_x, X, R, H, N)) return cudaErrorNotSupported;
