@@ -304,19 +304,49 @@ __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
 
 // 16-element block: codes in (q0, q1) (element 2i in the low nibble of byte
 // i), hidden row as 8 f16x2 words.  Unscaled fp32 sum.
+// E2M1 pair in byte J of `word` -> f16x2, the byte taken through a .b8
+// register view of the word (no shift / mask).
+template <int J>
+__device__ __forceinline__ uint32_t e2m1_byte_h2(uint32_t word) {
+    uint32_t h2;
+    if (J == 0)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+            : "=r"(h2) : "r"(word));
+    else if (J == 1)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+            : "=r"(h2) : "r"(word));
+    else if (J == 2)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+            : "=r"(h2) : "r"(word));
+    else
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+            : "=r"(h2) : "r"(word));
+    return h2;
+}
+
+template <int J>
+__device__ __forceinline__ void nvfp4_pair_fma(uint32_t word, uint32_t xh, float& a0, float& a1) {
+    const uint32_t w2 = e2m1_byte_h2<J>(word);
+    unsigned short wl, wh, xl, xhh;
+    split_h2(w2, wl, wh);
+    split_h2(xh, xl, xhh);
+    a0 = fma_f16_f32(wl, xl, a0);
+    a1 = fma_f16_f32(wh, xhh, a1);
+}
+
 __device__ __forceinline__ float nvfp4_block16(uint32_t q0, uint32_t q1, const uint32_t* xh) {
     float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t w2 = e2m1x2_to_h2(((j < 4 ? q0 : q1) >> (8 * (j & 3))) & 0xFFu);
-        unsigned short wl, wh, xl, xhh;
-        split_h2(w2, wl, wh);
-        split_h2(xh[j], xl, xhh);
-        a0 = fma_f16_f32(wl, xl, a0);
-        a1 = fma_f16_f32(wh, xhh, a1);
-    }
+    nvfp4_pair_fma<0>(q0, xh[0], a0, a1);
+    nvfp4_pair_fma<1>(q0, xh[1], a0, a1);
+    nvfp4_pair_fma<2>(q0, xh[2], a0, a1);
+    nvfp4_pair_fma<3>(q0, xh[3], a0, a1);
+    nvfp4_pair_fma<0>(q1, xh[4], a0, a1);
+    nvfp4_pair_fma<1>(q1, xh[5], a0, a1);
+    nvfp4_pair_fma<2>(q1, xh[6], a0, a1);
+    nvfp4_pair_fma<3>(q1, xh[7], a0, a1);
     return a0 + a1;
 }
+
 
 __device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
     uint32_t r;
@@ -588,6 +618,108 @@ __global__ void __launch_bounds__(kThreads, (CPL >= 4 ? 1 : 2)) k_gemv_nvfp4_dir
     finish_argmax<1>(b1, a);
 }
 
+
+// Same as k_gemv_nvfp4_direct with the prescaled f16 hidden row in shared
+// memory instead of registers (fewer registers -> more warps and more bytes
+// in flight).  Chunk c (64 elements = 8 pieces of 16 bytes) is stored with its
+// pieces XOR-swizzled by c % 8, so the 32 lanes of a warp (chunks c .. c+31)
+// read a block's two pieces without bank conflicts.
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t* r) {
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_gemv_nvfp4_xs(const GemvArgs a) {
+    extern __shared__ __align__(16) uint32_t xsh[];  // [nch][8 pieces][4 words], swizzled
+    __shared__ float s_xmax[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = a.H, nch = H >> 6;
+    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
+    const uint8_t* __restrict__ Wq = static_cast<const uint8_t*>(a.W);
+
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long r0 = gw * a.rows_per_warp;
+    const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
+
+    pdl_launch_dependents();
+    for (long long r = r0; r < min(r1, r0 + 2); ++r)
+        for (int c = lane; c < nch; c += 32) prefetch_l2(Wq + (size_t)r * qrow + c * 32);
+    pdl_wait();
+
+    float m = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) s_xmax[warp] = m;
+    __syncthreads();
+    float xmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) xmax = fmaxf(xmax, s_xmax[w]);
+    const int k = xmax > 0.f ? min(127, 141 - (int)((__float_as_uint(xmax) >> 23) & 0xFF)) : 0;
+    const float up = ldexpf(1.f, k), out_scale = a.g * ldexpf(1.f, -k);
+    for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {  // word i = elements 2i, 2i+1
+        const uint32_t pr = reinterpret_cast<const uint32_t*>(a.x)[i];
+        const int c = i >> 5, piece = (i >> 2) & 7, w = i & 3;
+        xsh[c * 32 + ((piece ^ (c & 7)) << 2) + w] = f32x2_to_h2(bf_lo(pr) * up, bf_hi(pr) * up);
+    }
+    __syncthreads();
+    const uint32_t xbase = ptx::smem_u32(xsh);
+
+    unsigned long long best = 0ull;
+    for (long long r = r0; r < r1; r += 2) {
+        const bool two = (r + 1 < r1);
+        U32x8 q0[2], q1[2];
+        uint32_t s0[2], s1[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                q0[j] = ld_stream32(Wq + (size_t)r * qrow + c * 32);
+                s0[j] = __ldg(reinterpret_cast<const uint32_t*>(a.scales + (size_t)r * srow) + c);
+                if (two) {
+                    q1[j] = ld_stream32(Wq + (size_t)(r + 1) * qrow + c * 32);
+                    s1[j] = __ldg(reinterpret_cast<const uint32_t*>(a.scales + (size_t)(r + 1) * srow) + c);
+                }
+            }
+        }
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // H <= 4096: at most two 64-element chunks per lane
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                const float2 a01 = e4m3x2_to_f2(s0[j] & 0xFFFFu), a23 = e4m3x2_to_f2(s0[j] >> 16);
+                const float2 b01 = two ? e4m3x2_to_f2(s1[j] & 0xFFFFu) : make_float2(0.f, 0.f);
+                const float2 b23 = two ? e4m3x2_to_f2(s1[j] >> 16) : make_float2(0.f, 0.f);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    uint32_t xv[8];
+                    lds128(xbase + (uint32_t)(c * 128 + (((2 * blk) ^ (c & 7)) << 4)), xv);
+                    lds128(xbase + (uint32_t)(c * 128 + (((2 * blk + 1) ^ (c & 7)) << 4)), xv + 4);
+                    const float sa = blk == 0 ? a01.x : blk == 1 ? a01.y : blk == 2 ? a23.x : a23.y;
+                    acc0 = fmaf(nvfp4_block16(q0[j].v[2 * blk], q0[j].v[2 * blk + 1], xv), sa, acc0);
+                    if (two) {
+                        const float sb = blk == 0 ? b01.x : blk == 1 ? b01.y : blk == 2 ? b23.x : b23.y;
+                        acc1 = fmaf(nvfp4_block16(q1[j].v[2 * blk], q1[j].v[2 * blk + 1], xv), sb, acc1);
+                    }
+                }
+            }
+        }
+        {
+            const float sc = warp_sum(acc0) * out_scale;
+            const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
+            const unsigned long long kk = make_key(sc, gid);
+            best = kk > best ? kk : best;
+        }
+        if (two) {
+            const float sc = warp_sum(acc1) * out_scale;
+            const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1);
+            const unsigned long long kk = make_key(sc, gid);
+            best = kk > best ? kk : best;
+        }
+    }
+    unsigned long long b1[1] = {best};
+    finish_argmax<1>(b1, a);
+}
+
 // ---------------------------------------------------------------------------
 // Block-scaled 4-bit head on CUDA cores, any B <= 8.  A lane chunk is 32 code
 // bytes = 64 elements = 4 scale blocks.  Each 16-element block is summed
@@ -746,6 +878,7 @@ cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* W
     a.x = x; a.W = Wq; a.scales = scales; a.g = g; a.cand = cand;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit;
     a.err = ws.ticket + 1;
+    if (nb == 1 && H <= 4096) return launch_split_v(k_gemv_nvfp4_xs, (size_t)H * 2, n_rows, a, s, true);
     if (nb == 1 && H <= 8192) {
         const int cpl = (H / 64 + 31) / 32;
         if (cpl <= 1) return launch_split_v(k_gemv_nvfp4_direct<1>, 0, n_rows, a, s, true);
