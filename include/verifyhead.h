@@ -202,6 +202,25 @@ VH_API vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void*
                                                  int B, int H, int Vc, int32_t* ids, float* maxlogit,
                                                  void* stream);
 
+/*
+ * Error word of the workspace.  The tensor-core kernels bound every internal
+ * wait (about 2 s); if one expires (e.g. the GPU is oversubscribed or another
+ * process holds its tensor memory) the kernel stops early, writes a nonzero
+ * 32-bit value at byte offset vh_workspace_error_offset() of `ws` (the same
+ * offset for every workspace size), and the outputs of that call are invalid.
+ * The library never clears this word: the caller may read it (one 4-byte
+ * copy) and reset it.
+ */
+VH_API size_t vh_workspace_error_offset(void);
+
+/*
+ * Self-test of that bounded-wait path: launches one CTA that waits on a
+ * barrier nothing completes, gives up after `timeout_us` microseconds
+ * (1..1,000,000), sets *flag |= 1 (device memory, 4-byte aligned) and
+ * returns.  The context stays usable.  No counterpart in the source pages.
+ */
+VH_API vh_status vh_selftest_bounded_wait(unsigned int* flag, unsigned int timeout_us, void* stream);
+
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
     VH_PATH_AUTO = 0,      /* tensor cores when B*(k+1) > 8 and H % 64 == 0, else CUDA cores */

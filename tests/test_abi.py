@@ -47,6 +47,7 @@ def test_status_strings_and_workspace(vh):
     assert vh.vh_workspace_bytes(1) == 32
     assert vh.vh_workspace_bytes(256) == 256 * 8 + 16
     assert vh.vh_workspace_bytes(3) % 16 == 0
+    assert vh.lib().vh_workspace_error_offset() == 4
 
 
 # Fake, aligned, never-dereferenced addresses: argument checks run before any

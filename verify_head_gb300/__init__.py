@@ -33,7 +33,8 @@ VH_PATH_TENSOR = 2
 EXPORTS = (
     "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
-    "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather",
+    "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather", "vh_workspace_error_offset",
+    "vh_selftest_bounded_wait",
 )
 
 
@@ -71,6 +72,10 @@ def lib():
         L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
         L.spec_verify_greedy.restype = i32
         L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.vh_workspace_error_offset.restype = sz
+        L.vh_workspace_error_offset.argtypes = []
+        L.vh_selftest_bounded_wait.restype = i32
+        L.vh_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
         L.mtp_draft_head_argmax_gather.restype = i32
         L.mtp_draft_head_argmax_gather.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         L.mtp_draft_head_argmax_static_ws.restype = i32
@@ -87,6 +92,13 @@ def status_string(status: int) -> str:
 
 def vh_workspace_bytes(rows: int) -> int:
     return int(lib().vh_workspace_bytes(int(rows)))
+
+
+def workspace_error(ws) -> int:
+    """The error word of a workspace tensor (nonzero: a bounded wait expired in
+    some call that used it).  Copies 4 bytes to the host (synchronising)."""
+    off = int(lib().vh_workspace_error_offset())
+    return int(ws[off:off + 4].cpu().view(__import__("torch").int32).item())
 
 
 def _check(status: int, where: str):

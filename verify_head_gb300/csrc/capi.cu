@@ -40,12 +40,7 @@ vh_status check_device() {
     return VH_OK;
 }
 
-vh::Workspace make_ws(void* ws, int rows) {
-    vh::Workspace w;
-    w.keys = static_cast<unsigned long long*>(ws);
-    w.ticket = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + vh::ws_keys_bytes(rows));
-    return w;
-}
+vh::Workspace make_ws(void* ws, int /*rows*/) { return vh::ws_view(ws); }
 
 vh_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return VH_OK;

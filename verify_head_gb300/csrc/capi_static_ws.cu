@@ -87,9 +87,7 @@ vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand
         cudaGetLastError();
         return VH_ERR_LAUNCH;
     }
-    vh::Workspace w;
-    w.keys = static_cast<unsigned long long*>(scratch);
-    w.ticket = reinterpret_cast<unsigned int*>(static_cast<char*>(scratch) + vh::ws_keys_bytes(B));
+    const vh::Workspace w = vh::ws_view(scratch);
     int grp = 8;
     while (grp > 1 && (size_t)grp * H * 2 > 131072) grp /= 2;
     const uint16_t* x = static_cast<const uint16_t*>(hidden);

@@ -59,15 +59,27 @@ __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u <<
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
-// Workspace: keys[rows] (uint64) followed by a uint32 ticket counter.  The
-// caller zeroes it once; every kernel leaves it zeroed again.
+// Workspace layout: a 16-byte header (uint32 ticket counter at byte 0, uint32
+// error word at byte 4, 8 bytes unused) followed by keys[rows] (uint64).  The
+// caller zeroes it once; every kernel leaves ticket and keys zeroed again.
+// The error word is only ever set (by a wait that gave up), never cleared.
 
 struct Workspace {
     unsigned long long* keys;
-    unsigned int* ticket;
+    unsigned int* ticket;  // ticket[1] is the error word
 };
 
+constexpr size_t kWsHeaderBytes = 16;
+constexpr size_t kWsErrorOffset = 4;
 __host__ __device__ constexpr size_t ws_keys_bytes(int rows) { return ((size_t)rows * 8 + 15) / 16 * 16; }
-__host__ __device__ constexpr size_t ws_total_bytes(int rows) { return ws_keys_bytes(rows) + 16; }
+__host__ __device__ constexpr size_t ws_total_bytes(int rows) { return kWsHeaderBytes + ws_keys_bytes(rows); }
+
+// Views of a workspace base pointer (the row count does not move anything).
+__host__ __device__ inline Workspace ws_view(void* base) {
+    Workspace w;
+    w.ticket = static_cast<unsigned int*>(base);
+    w.keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(base) + kWsHeaderBytes);
+    return w;
+}
 
 }  // namespace vh
