@@ -341,6 +341,8 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"
         out["gather"] = measure_gather(torch, vh, synth, timer, peaks)
     if only in ("all", "chain"):
         out["chain_graph"] = measure_chain_graph(torch, vh, synth, timer, peaks)
+    if only in ("all", "verify_nvfp4"):
+        out["verify_nvfp4"] = measure_verify_nvfp4(torch, vh, synth, timer, peaks)
     if only in ("all", "nvfp4"):
         out["nvfp4"] = measure_nvfp4(torch, vh, synth, timer, peaks)
     return out
@@ -467,6 +469,23 @@ def measure_chain_graph(torch, vh, synth, timer, peaks):
             "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
+def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
+    """Greedy verify of 4 sequences x 4 positions over the 65,536 x 4096 4-bit head."""
+    dev = torch.device("cuda")
+    c = synth.nvfp4_case(Vc=65_536, H=4096, B=1, steps=1, seed=5)
+    q = torch.from_numpy(c.q).to(dev)
+    s = torch.from_numpy(c.s).to(dev)
+    X = torch.from_numpy(synth.normal_bf16(7, synth.STREAM_VHIDDEN, (16, 4096), 1.0).view(np.int16)).to(dev)
+    d = torch.zeros((4, 3), dtype=torch.int32, device=dev)
+    ws = vh.workspace(16)
+    us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(X, q, s, c.g, d, 4, 3, ws=ws), 20)
+    med = statistics.median(us)
+    nbytes = c.q.nbytes + c.s.nbytes + 16 * 4096 * 2
+    return {"workload": "4 seqs x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "rounds_per_s": round(1e6 / med, 1),
+            **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
 def measure_nvfp4(torch, vh, synth, timer, peaks):
     dev = torch.device("cuda")
 
@@ -560,7 +579,7 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "draft", "verify", "sweep", "nvfp4", "gather", "chain"],
+                    choices=["all", "draft", "verify", "sweep", "nvfp4", "gather", "chain", "verify_nvfp4"],
                     help="all = the bench line; others run one measurement only (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -221,6 +221,30 @@ VH_API size_t vh_workspace_error_offset(void);
  */
 VH_API vh_status vh_selftest_bounded_wait(unsigned int* flag, unsigned int timeout_us, void* stream);
 
+/*
+ * Greedy speculative verification over a block-scaled 4-bit full head (the
+ * NVFP4 format of mtp_draft_head_argmax_nvfp4, rows = the V vocabulary
+ * entries).  Rows, next_ids, row_maxlogit and accept_len are defined as for
+ * spec_verify_greedy, with W_full replaced by the decoded 4-bit head.
+ *
+ * The head is a quarter of the bf16 head's bytes, so few verified rows
+ * (B*(k+1) <= 16 per tensor-core pass) read 4x less memory.  Rows are
+ * processed in groups of 16 on the tensor cores (H % 512 == 0) or 8 on CUDA
+ * cores (other H); every group reads the head once, so large batches are
+ * better served by the bf16 head (spec_verify_greedy), which is
+ * tensor-bound at 256 rows either way.
+ *
+ *  hidden        device, bf16 [B*(k+1)][H], 16-byte aligned
+ *  Wq, scales    device, uint8 [V][H/2] (32-byte aligned), uint8 [V][H/16] (16-byte aligned)
+ *  tensor_scale  finite, > 0
+ *  B, k, V       as for spec_verify_greedy;  H: 64 <= H <= 65536, H % 64 == 0
+ *  draft_ids, accept_len, next_ids, row_maxlogit, ws: as for spec_verify_greedy
+ */
+VH_API vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                          float tensor_scale, const int32_t* draft_ids, int B, int k, int H, int V,
+                                          int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
+                                          size_t ws_bytes, void* stream);
+
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
     VH_PATH_AUTO = 0,      /* tensor cores when B*(k+1) > 8 and H % 64 == 0, else CUDA cores */

@@ -18,6 +18,8 @@ Parity status per function (what pins it; see tests/test_oracle_pins.py):
                       draft_argmax on an exactly representable head
   draft_argmax_gather exact-integer brute force with unsorted and repeated
                       ids, equality with draft_argmax on the sorted set
+  verify_greedy_nvfp4 equality with verify_greedy on an exactly representable
+                      head (g = 1), hand-built acceptance fixtures
   verify_greedy       exact-integer brute force, hand-built acceptance
                       fixtures (tests/golden/accept_cases.txt), equality with
                       draft_argmax over the identity candidate set
@@ -82,6 +84,9 @@ def lib():
         L.vh_oracle_accept_len.restype = ctypes.c_int32
         L.vh_oracle_verify_greedy.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i64, vp, vp, vp, vp, i32]
         L.vh_oracle_verify_greedy.restype = i32
+        L.vh_oracle_verify_greedy_nvfp4.argtypes = [vp, vp, vp, f32, vp, i64, i64, i64, i64, vp, i64, vp, vp, vp,
+                                                    vp, i32]
+        L.vh_oracle_verify_greedy_nvfp4.restype = i32
         L.vh_oracle_scores_bf16.argtypes = [vp, vp, i64, i64, vp, i32]
         L.vh_oracle_scores_nvfp4.argtypes = [vp, vp, vp, f32, i64, i64, vp, i32]
         L.vh_oracle_decode_nvfp4.argtypes = [vp, vp, f32, i64, i64, vp]
@@ -202,6 +207,34 @@ def verify_greedy(X, W, draft_ids, B: int, k: int, rows=None, nthreads: int | No
                                        ml.ctypes.data, sec.ctypes.data, nthreads or threads())
     if rc != 0:
         raise ValueError(f"oracle verify_greedy failed ({rc})")
+    return (acc if (rows is None and d is not None) else None), nid, ml, sec
+
+
+def verify_greedy_nvfp4(X, q, s, g, draft_ids, B: int, k: int, rows=None, nthreads: int | None = None):
+    """As verify_greedy with the 4-bit head (q [V,H/2], s [V,H/16], g)."""
+    X, pX = _c(X, np.uint16)
+    q, pq = _c(q, np.uint8)
+    s, ps = _c(s, np.uint8)
+    R, H = X.shape
+    V = q.shape[0]
+    assert R == B * (k + 1) and q.shape[1] * 2 == H and s.shape == (V, H // 16)
+    if draft_ids is not None:
+        d, pd = _c(draft_ids, np.int32)
+    else:
+        d, pd = None, None
+    nid = np.full(R, -1, np.int32)
+    ml = np.full(R, np.nan, np.float32)
+    sec = np.full(R, np.nan, np.float32)
+    acc = np.empty(B, np.int32)
+    if rows is not None:
+        rr, pr = _c(rows, np.int32)
+        nr = rr.size
+    else:
+        rr, pr, nr = None, None, 0
+    rc = lib().vh_oracle_verify_greedy_nvfp4(pX, pq, ps, float(g), pd, B, k, H, V, pr, nr, nid.ctypes.data,
+                                             acc.ctypes.data, ml.ctypes.data, sec.ctypes.data, nthreads or threads())
+    if rc != 0:
+        raise ValueError(f"oracle verify_greedy_nvfp4 failed ({rc})")
     return (acc if (rows is None and d is not None) else None), nid, ml, sec
 
 

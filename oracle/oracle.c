@@ -282,6 +282,34 @@ int vh_oracle_verify_greedy(const uint16_t* X, const uint16_t* W, const int32_t*
     return 0;
 }
 
+/* Greedy verify over a block-scaled 4-bit full head (codes q [V][H/2],
+ * scales s [V][H/16], tensor scale g): the same rules as the bf16 verify,
+ * every weight decoded as e2m1(q) * e4m3(s) * g. */
+int vh_oracle_verify_greedy_nvfp4(const uint16_t* X, const uint8_t* q, const uint8_t* s, float g,
+                                  const int32_t* draft, int64_t B, int64_t k, int64_t H, int64_t V,
+                                  const int32_t* rows, int64_t nrows, int32_t* next_ids, int32_t* accept_len,
+                                  float* maxlogit, float* second, int nthreads) {
+    if (B < 1 || k < 0 || H < 16 || H % 16 != 0 || V < 1) return -1;
+    const int64_t R = B * (k + 1);
+    float* sc = (float*)malloc((size_t)V * sizeof(float));
+    if (!sc) return -2;
+    const int64_t n = rows ? nrows : R;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        if (r < 0 || r >= R) { free(sc); return -1; }
+        all_scores(X + r * H, NULL, q, s, g, V, H, sc, nthreads);
+        float bv, sv;
+        int64_t v = first_argmax(sc, V, &bv, &sv);
+        next_ids[r] = (int32_t)v;
+        if (maxlogit) maxlogit[r] = bv;
+        if (second) second[r] = sv;
+    }
+    free(sc);
+    if (!rows && accept_len && draft)
+        for (int64_t b = 0; b < B; ++b) accept_len[b] = vh_oracle_accept_len(next_ids + b * (k + 1), draft + b * k, k);
+    return 0;
+}
+
 /* All scores of one hidden row against a bf16 head (for near-tie checks). */
 void vh_oracle_scores_bf16(const uint16_t* x, const uint16_t* W, int64_t n, int64_t H, float* out, int nthreads) {
     all_scores(x, W, NULL, NULL, 0.0f, n, H, out, nthreads);

@@ -495,3 +495,70 @@ def test_error_status_on_gpu(vh):
                               torch.zeros(10, 80, dtype=torch.bfloat16, device="cuda"),
                               torch.zeros(1, 3, dtype=torch.int32, device="cuda"), 1, 3, path=vh.VH_PATH_TENSOR)
     assert e.value.status == vh.VH_ERR_SHAPE  # tensor path needs H % 64 == 0
+
+
+# ----------------------------------------------------------------------------
+# greedy verify over a 4-bit head
+
+
+def run_verify_nvfp4(vh, X, q, s, g, draft, B, k):
+    import torch
+    acc, nid, ml = vh.spec_verify_greedy_nvfp4(to_torch_bf16(X), to_torch(q), to_torch(s), g, to_torch(draft), B, k)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), nid.cpu().numpy(), ml.cpu().numpy()
+
+
+def check_verify_nvfp4(vh, orc, syn, X, q, s, g, B, k, seed):
+    V = q.shape[0]
+    _, o_nid, o_ml, o_sec = orc.verify_greedy_nvfp4(X, q, s, g, None, B, k)
+    draft = syn.corrupt_ids(seed, syn.STREAM_CORRUPT, o_nid.reshape(B, k + 1)[:, :k].copy(), V, 0.45)
+    o_acc = np.array([orc.accept_len(o_nid[b * (k + 1): b * (k + 1) + k], draft[b]) for b in range(B)], np.int32)
+    g_acc, g_nid, g_ml = run_verify_nvfp4(vh, X, q, s, g, draft, B, k)
+
+    def score_of(r, v):
+        return float(orc.scores_nvfp4(X[r], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0])
+
+    check_ids(g_nid, g_ml, o_nid, o_ml, o_sec, score_of, TOL_4BIT)
+    check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
+
+
+@pytest.mark.parametrize("B,k,V,H", [(1, 3, 1000, 512), (4, 3, 3000, 1024), (5, 3, 2000, 512), (3, 2, 700, 256),
+                                     (2, 1, 129, 64), (16, 3, 1500, 512)])
+def test_verify_nvfp4_shapes(vh, orc, syn, B, k, V, H):
+    w = syn.normal_f32(V + H, 6, (V, H), 0.02)
+    q, s, g = syn.nvfp4_quantize(w)
+    X = syn.normal_bf16(B + k, 4, (B * (k + 1), H), 1.0)
+    check_verify_nvfp4(vh, orc, syn, X, q, s, g, B, k, seed=V)
+
+
+def test_verify_nvfp4_full_head_65536x4096(vh, orc, syn):
+    """4 sequences x 4 positions against the 65,536 x 4096 4-bit head."""
+    c = syn.nvfp4_case(Vc=65_536, H=4096, B=1, steps=1, seed=5)
+    X = syn.normal_bf16(7, syn.STREAM_VHIDDEN, (16, 4096), 1.0)
+    check_verify_nvfp4(vh, orc, syn, X, c.q, c.s, c.g, 4, 3, seed=7)
+
+
+def test_verify_nvfp4_accept_cases(vh):
+    cases = []
+    with open(os.path.join(HERE, "golden", "accept_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, nxt, dr, a, _ = [p.split() for p in line.split("|")]
+                if int(k[0]) == 3:
+                    cases.append(([int(v) for v in nxt], [int(v) for v in dr], int(a[0])))
+    V = H = 512
+    q = np.zeros((V, H // 2), np.uint8)
+    for v in range(V):
+        q[v, v // 2] = 0x02 if v % 2 == 0 else 0x20  # one-hot 4-bit head: weight 1.0 at h == v
+    s = np.full((V, H // 16), 0x38, np.uint8)
+    B, k = len(cases), 3
+    X = np.full((B * (k + 1), H), 0xBF80, np.uint16)
+    draft = np.zeros((B, k), np.int32)
+    for b, (nxt, dr, _) in enumerate(cases):
+        for j, t in enumerate(nxt):
+            X[b * (k + 1) + j, t] = 0x4000
+        draft[b] = dr
+    acc, nid, _ = run_verify_nvfp4(vh, X, q, s, 1.0, draft, B, k)
+    assert list(acc) == [c[2] for c in cases]
+    assert list(nid) == [t for c in cases for t in c[0]]

@@ -431,3 +431,38 @@ def test_gather_equals_sorted_candidate_table(oracle_mod, synth_mod):
     b = oracle_mod.draft_argmax(x, np.ascontiguousarray(W_full[uniq]), uniq)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_nvfp4_verify_equals_bf16_verify_on_representable_head(oracle_mod):
+    rng = np.random.default_rng(21)
+    V, H, B, k = 300, 64, 3, 3
+    q = rng.integers(0, 256, size=(V, H // 2), dtype=np.uint8)
+    s = rng.integers(0x20, 0x48, size=(V, H // 16), dtype=np.uint8)
+    Wb = bf16_bits(oracle_mod.decode_nvfp4(q, s, 1.0))
+    X = (rng.standard_normal((B * (k + 1), H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    draft = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    a = oracle_mod.verify_greedy_nvfp4(X, q, s, 1.0, draft, B, k)
+    b = oracle_mod.verify_greedy(X, Wb, draft, B, k)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+
+
+def test_nvfp4_verify_acceptance_fixtures(oracle_mod):
+    """One-hot 4-bit head (code 2 = 1.0, scale 0x38 = 1.0): row j's greedy id is
+    the position of its peak; the hand-built acceptance cases must hold."""
+    cases = [c for c in _parse_accept_cases() if c[0] == 3]
+    V = H = 64
+    q = np.zeros((V, H // 2), np.uint8)
+    for v in range(V):
+        q[v, v // 2] = 0x02 if v % 2 == 0 else 0x20
+    s = np.full((V, H // 16), 0x38, np.uint8)
+    B, k = len(cases), 3
+    X = np.full((B * (k + 1), H), -1.0, np.float32)
+    draft = np.zeros((B, k), np.int32)
+    for b, (_, nxt, dr, _, _) in enumerate(cases):
+        for j, t in enumerate(nxt):
+            X[b * (k + 1) + j, t] = 2.0
+        draft[b] = dr
+    acc, nid, _, _ = oracle_mod.verify_greedy_nvfp4(bf16_bits(X), q, s, 1.0, draft, B, k)
+    assert list(acc) == [c[3] for c in cases]
+    assert list(nid) == [t for c in cases for t in c[1]]

@@ -34,7 +34,7 @@ EXPORTS = (
     "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
     "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather", "vh_workspace_error_offset",
-    "vh_selftest_bounded_wait",
+    "vh_selftest_bounded_wait", "spec_verify_greedy_nvfp4",
 )
 
 
@@ -72,6 +72,9 @@ def lib():
         L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
         L.spec_verify_greedy.restype = i32
         L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.spec_verify_greedy_nvfp4.restype = i32
+        L.spec_verify_greedy_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                               vp]
         L.vh_workspace_error_offset.restype = sz
         L.vh_workspace_error_offset.argtypes = []
         L.vh_selftest_bounded_wait.restype = i32
@@ -225,4 +228,30 @@ def spec_verify_greedy(hidden, W_full, draft_ids, B: int, k: int, accept_len=Non
                                        _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws), ws.numel(), _stream_ptr(stream),
                                        int(path))
     _check(st, "spec_verify_greedy")
+    return accept_len, next_ids, row_maxlogit
+
+
+def spec_verify_greedy_nvfp4(hidden, Wq, scales, tensor_scale, draft_ids, B: int, k: int, accept_len=None,
+                             next_ids=None, row_maxlogit=None, ws=None, stream=None, want_maxlogit: bool = True):
+    """hidden [B*(k+1),H] bf16, Wq [V,H/2] uint8, scales [V,H/16] uint8, draft_ids [B,k] int32
+    -> (accept_len [B], next_ids [B*(k+1)], row_maxlogit or None)."""
+    torch = _torch()
+    _require_cuda(hidden, Wq, scales, draft_ids)
+    R, H = hidden.shape
+    V = Wq.shape[0]
+    if R != B * (k + 1) or Wq.shape[1] * 2 != H or tuple(scales.shape) != (V, H // 16) or draft_ids.numel() != B * k:
+        raise ValueError("shape mismatch")
+    dev = hidden.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_ids is None:
+        next_ids = torch.empty(R, dtype=torch.int32, device=dev)
+    if row_maxlogit is None and want_maxlogit:
+        row_maxlogit = torch.empty(R, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(R, dev)
+    st = lib().spec_verify_greedy_nvfp4(_ptr(hidden), _ptr(Wq), _ptr(scales), float(tensor_scale), _ptr(draft_ids), B,
+                                        k, H, V, _ptr(accept_len), _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws),
+                                        ws.numel(), _stream_ptr(stream))
+    _check(st, "spec_verify_greedy_nvfp4")
     return accept_len, next_ids, row_maxlogit

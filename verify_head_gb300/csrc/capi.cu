@@ -193,6 +193,45 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     return VH_OK;
 }
 
+vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales, float tensor_scale,
+                                   const int32_t* draft_ids, int B, int k, int H, int V, int32_t* accept_len,
+                                   int32_t* next_ids, float* row_maxlogit, void* ws, size_t ws_bytes, void* stream) {
+    if (!hidden || !Wq || !scales || !draft_ids || !accept_len || !next_ids || !ws) return VH_ERR_NULL;
+    if (B < 1 || k < 1 || k > 15 || H < 64 || H > kMaxH || H % 64 != 0 || V < 1) return VH_ERR_SHAPE;
+    if ((long long)B * (k + 1) > 65536) return VH_ERR_SHAPE;
+    if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.0e38f)) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(Wq, 32) || !aligned(scales, 16) || !aligned(draft_ids, 4) ||
+        !aligned(accept_len, 4) || !aligned(next_ids, 4) || !aligned(row_maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    const int R = B * (k + 1);
+    if (ws_bytes < vh_workspace_bytes(R)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, R);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const bool tc = (H % 512 == 0);
+    const int grp = tc ? kTcFp4Rows : gemv_group(H);
+    for (int r0 = 0; r0 < R; r0 += grp) {
+        const int nr = std::min(grp, R - r0);
+        vh::AcceptTail tail;
+        if (r0 + nr == R) {  // the final group also runs the acceptance scan
+            tail.draft = draft_ids;
+            tail.next_ids = next_ids;
+            tail.accept_len = accept_len;
+            tail.B = B;
+            tail.k = k;
+        }
+        float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
+        cudaError_t e = tc ? vh::launch_nvfp4_tc(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, nullptr, V, w,
+                                                 next_ids + r0, ml, s, tail)
+                           : vh::launch_gemv_nvfp4(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, nullptr, V, w,
+                                                   next_ids + r0, ml, s, tail);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
 vh_status spec_verify_greedy(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k, int H,
                              int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
                              size_t ws_bytes, void* stream) {

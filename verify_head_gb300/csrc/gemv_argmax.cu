@@ -873,10 +873,10 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
 
 cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
                               const int32_t* cand, int n_rows, Workspace ws, int32_t* ids, float* maxlogit,
-                              cudaStream_t s) {
+                              cudaStream_t s, const AcceptTail& tail) {
     GemvArgs a{};
     a.x = x; a.W = Wq; a.scales = scales; a.g = g; a.cand = cand;
-    a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit;
+    a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit; a.tail = tail;
     a.err = ws.ticket + 1;
     if (nb == 1 && H <= 4096) return launch_split_v(k_gemv_nvfp4_xs, (size_t)H * 2, n_rows, a, s, true);
     if (nb == 1 && H <= 8192) {

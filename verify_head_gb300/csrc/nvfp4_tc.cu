@@ -86,7 +86,8 @@ struct Args {
     Workspace ws;
     unsigned int* err;
     int32_t* ids;
-    float* maxlogit;
+    float* maxlogit;  // nullable
+    AcceptTail tail;  // acceptance scan by the last CTA (draft == nullptr: none)
 };
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, unsigned long long* bar, int x, int y,
@@ -482,9 +483,21 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
     if (threadIdx.x < a.nb) {
         const unsigned long long k = atomicExch(a.ws.keys + threadIdx.x, 0ull);
         a.ids[threadIdx.x] = (int32_t)key_gid(k);
-        a.maxlogit[threadIdx.x] = key_score(k);
+        if (a.maxlogit != nullptr) a.maxlogit[threadIdx.x] = key_score(k);
     }
     if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
+    if (a.tail.draft != nullptr) {
+        __threadfence();
+        __syncthreads();
+        const int k = a.tail.k;
+        for (int b = threadIdx.x; b < a.tail.B; b += blockDim.x) {
+            const volatile int32_t* nid = a.tail.next_ids + (size_t)b * (k + 1);
+            const int32_t* d = a.tail.draft + (size_t)b * k;
+            int acc = 0;
+            while (acc < k && nid[acc] == d[acc]) ++acc;
+            a.tail.accept_len[b] = acc;
+        }
+    }
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -546,7 +559,8 @@ static bool make_map_u8(CUtensorMap* m, const void* base, int rows, int cols, in
 }  // namespace fp4tc
 
 cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
-                            const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s) {
+                            const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
+                            const AcceptTail& tail) {
     using namespace fp4tc;
     if (nb < 1 || nb > kN || H < kKs || H % kKs != 0 || Vc < 1) return cudaErrorNotSupported;  // H % 512 == 0
     alignas(64) CUtensorMap map_q, map_s, map_x;
@@ -568,6 +582,7 @@ cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq,
     a.err = ws.ticket + 1;
     a.ids = ids;
     a.maxlogit = maxlogit;
+    a.tail = tail;
     const int grid = std::max(1, std::min(sm_count(), a.n_tiles));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);

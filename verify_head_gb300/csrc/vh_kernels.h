@@ -30,13 +30,14 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
 // GEMV + argmax on CUDA cores, nb <= 8.
 cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
                               const int32_t* cand, int n_rows, Workspace ws, int32_t* ids, float* maxlogit,
-                              cudaStream_t s);
+                              cudaStream_t s, const AcceptTail& tail = AcceptTail{});
 
 // Block-scaled 4-bit head on the tensor cores (exact f16 dequantisation,
 // tcgen05 kind::f16), nb <= 16 hidden rows, H % 256 == 0.  Returns
 // cudaErrorNotSupported for other shapes.
 cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
-                            const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s);
+                            const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
+                            const AcceptTail& tail = AcceptTail{});
 
 // tcgen05 skinny GEMM + per-row argmax + acceptance scan for R <= 256 hidden
 // rows (H % 64 == 0).  Returns cudaErrorNotSupported when the shape does not
