@@ -27,16 +27,19 @@ inline int gemv_group(int H) {
 }
 
 vh_status check_device() {
+    static int ok_cache[64] = {};  // 1: device already checked
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         cudaGetLastError();
         return VH_ERR_DEVICE;
     }
+    if (dev < 64 && ok_cache[dev]) return VH_OK;
     int major = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess || major < 10) {
         cudaGetLastError();
         return VH_ERR_DEVICE;
     }
+    if (dev < 64) ok_cache[dev] = 1;
     return VH_OK;
 }
 

@@ -813,10 +813,16 @@ __global__ void __launch_bounds__(kThreads) k_gemv_nvfp4(const GemvArgs a) {
 // ---------------------------------------------------------------------------
 // Host launchers.
 
+// Per-device launch facts, looked up once (device ordinals below kMaxDev).
+constexpr int kMaxDev = 64;
+
 int sm_count() {
+    static int cache[kMaxDev] = {};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev && cache[dev] > 0) return cache[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev) cache[dev] = n;
     return n;
 }
 
@@ -826,9 +832,22 @@ static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
+    // resident CTAs per SM for this kernel and shared-memory size (cached per device)
+    static int occ_cache[kMaxDev] = {};
+    static size_t occ_smem[kMaxDev] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
-    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDev && occ_cache[dev] > 0 && occ_smem[dev] == smem) {
+        per_sm = occ_cache[dev];
+    } else {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDev) {
+            occ_smem[dev] = smem;
+            occ_cache[dev] = per_sm;
+        }
+    }
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
     // one resident wave; each warp gets a contiguous, equal share of rows
