@@ -480,8 +480,35 @@ def measure_chain_graph(torch, vh, synth, timer, peaks):
 
 
 def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
-    """Greedy verify of 4 sequences x 4 positions over the 65,536 x 4096 4-bit head."""
+    """Greedy verify over 4-bit heads: 64 sequences x 4 positions against the
+    full 248,320 x 2048 head (CTA-pair kernel), and 4 x 4 rows against the
+    65,536 x 4096 head (16-row kernel)."""
     dev = torch.device("cuda")
+    out = {}
+    # full head, 256 rows
+    q, s, g = synth.nvfp4_head(seed=2, V=synth.V_FULL, H=2048)
+    X = synth.verify_case(B=64, k=3, H=2048, V=synth.V_FULL, seed=4, with_head=False).X
+    dq, ds = torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev)
+    dX = torch.from_numpy(X.view(np.int16)).to(dev)
+    d = torch.from_numpy(synth.corrupt_ids(11, synth.STREAM_CORRUPT, np.zeros((64, 3), np.int32), synth.V_FULL,
+                                           1.0)).to(dev)
+    ws = vh.workspace(256)
+    us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(dX, dq, ds, g, d, 64, 3, ws=ws), 10)
+    med = statistics.median(us)
+    nbytes = q.nbytes + s.nbytes + X.nbytes
+    flops = 2.0 * 256 * synth.V_FULL * 2048
+    out["full_head_256_rows"] = {
+        "workload": "64 seqs x 4 rows x 2048 bf16 vs the full 248,320 x 2048 4-bit head (seed 2; hidden seed 4; "
+                    "draft ids uniform, so acceptance is not reported)",
+        "kernel": "k_verify_fp4_pair<256> (CTA pair, exact bf16 dequantisation in shared memory, tcgen05 cta_group::2)",
+        "rounds_per_s": round(1e6 / med, 1), **stats(us),
+        "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+        "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+        "tflops": round(flops / (med * 1e-6) / 1e12, 1),
+        "tensor_frac_burst": round(flops / (med * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+        "algorithmic_bytes_per_launch": nbytes}
+    del dq, ds, dX
+    # 16 rows vs the 65,536 x 4096 head
     c = synth.nvfp4_case(Vc=65_536, H=4096, B=1, steps=1, seed=5)
     q = torch.from_numpy(c.q).to(dev)
     s = torch.from_numpy(c.s).to(dev)
@@ -491,9 +518,11 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
     us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(X, q, s, c.g, d, 4, 3, ws=ws), 20)
     med = statistics.median(us)
     nbytes = c.q.nbytes + c.s.nbytes + 16 * 4096 * 2
-    return {"workload": "4 seqs x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "rounds_per_s": round(1e6 / med, 1),
-            **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
-            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    out["head_65536x4096_16_rows"] = {
+        "workload": "4 seqs x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "kernel": "k_nvfp4_tc",
+        "rounds_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+        "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    return out
 
 
 def measure_nvfp4(torch, vh, synth, timer, peaks):

@@ -284,6 +284,12 @@ def nvfp4_case(Vc: int = 65_536, H: int = 4096, B: int = 1, steps: int = 3, seed
                      {"V": V, "seed": seed})
 
 
+def nvfp4_head(seed: int = 2, V: int = V_FULL, H: int = 2048):
+    """Block-scaled 4-bit full head: the fp32 N(0, 0.02) rows of stream W4
+    (seed `seed`) encoded as in nvfp4_case -> (codes, scales, g)."""
+    return nvfp4_quantize(normal_f32(seed, STREAM_W4, (V, H), 0.02))
+
+
 def gather_row_ids(seed: int = 6, V: int = V_FULL, n_fixed: int = 32_768, n_dynamic: int = 16_384,
                    step: int = 0) -> np.ndarray:
     """Candidate rows read in place from the full head: a fixed sorted set of

@@ -522,8 +522,13 @@ def check_verify_nvfp4(vh, orc, syn, X, q, s, g, B, k, seed):
     check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
 
 
+# rows <= 16: one k_nvfp4_tc pass; 17..128 rows: CTA pair with N = 128; 129..256:
+# N = 256; > 256 rows: groups of 256; H = 2048 wraps the raw-code ring along K;
+# V = 40,000 gives every CTA pair several tiles (accumulator double buffering)
 @pytest.mark.parametrize("B,k,V,H", [(1, 3, 1000, 512), (4, 3, 3000, 1024), (5, 3, 2000, 512), (3, 2, 700, 256),
-                                     (2, 1, 129, 64), (16, 3, 1500, 512)])
+                                     (2, 1, 129, 64), (16, 3, 1500, 512), (33, 3, 2500, 512), (64, 3, 1100, 1024),
+                                     (75, 3, 900, 512), (16, 3, 3000, 2048), (20, 3, 40_000, 512),
+                                     (7, 15, 1300, 512)])
 def test_verify_nvfp4_shapes(vh, orc, syn, B, k, V, H):
     w = syn.normal_f32(V + H, 6, (V, H), 0.02)
     q, s, g = syn.nvfp4_quantize(w)
@@ -536,6 +541,35 @@ def test_verify_nvfp4_full_head_65536x4096(vh, orc, syn):
     c = syn.nvfp4_case(Vc=65_536, H=4096, B=1, steps=1, seed=5)
     X = syn.normal_bf16(7, syn.STREAM_VHIDDEN, (16, 4096), 1.0)
     check_verify_nvfp4(vh, orc, syn, X, c.q, c.s, c.g, 4, 3, seed=7)
+
+
+def test_verify_nvfp4_full_head_248320x2048(vh, orc, syn):
+    """64 sequences x 4 positions against the full 248,320 x 2048 4-bit head
+    (the CTA-pair kernel's launch in the bench).  The live oracle scores the
+    rows of three sequences; their draft ids are the oracle's greedy ids
+    corrupted w.p. 0.45, the other sequences' draft ids are uniform ids."""
+    B, k, V = 64, 3, syn.V_FULL
+    q, s, g = syn.nvfp4_head(seed=2, V=V, H=2048)
+    X = syn.verify_case(B=B, k=k, H=2048, V=V, seed=4, with_head=False).X
+    seqs = [0, 29, 63]
+    rows = np.array([b * (k + 1) + j for b in seqs for j in range(k + 1)], np.int32)
+    _, o_nid, o_ml, o_sec = orc.verify_greedy_nvfp4(X, q, s, g, None, B, k, rows=rows)
+    draft = syn.corrupt_ids(11, syn.STREAM_CORRUPT, np.zeros((B, k), np.int32), V, 1.0)  # uniform ids != 0
+    truth = np.stack([o_nid[b * (k + 1): b * (k + 1) + k] for b in seqs])
+    draft[seqs] = syn.corrupt_ids(12, syn.STREAM_CORRUPT, truth, V, 0.45)
+    g_acc, g_nid, g_ml = run_verify_nvfp4(vh, X, q, s, g, draft, B, k)
+    np.testing.assert_array_equal(g_acc, accept_scan(g_nid, draft, B, k))
+    assert np.all((g_nid >= 0) & (g_nid < V))
+
+    def score_of(r, v):
+        return float(orc.scores_nvfp4(X[rows[r]], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0])
+
+    check_ids(g_nid[rows], g_ml[rows], o_nid[rows], o_ml[rows], o_sec[rows], score_of, TOL_4BIT)
+    for i, b in enumerate(seqs):
+        o_acc = orc.accept_len(o_nid[b * (k + 1): b * (k + 1) + k], draft[b])
+        r = rows[i * (k + 1): i * (k + 1) + min(o_acc, k - 1) + 1]
+        if all(float(o_ml[x]) - float(o_sec[x]) > 1e-2 for x in r):
+            assert g_acc[b] == o_acc, (b, g_acc[b], o_acc)
 
 
 def test_verify_nvfp4_accept_cases(vh):

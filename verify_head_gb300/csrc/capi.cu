@@ -214,6 +214,27 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
     const vh::Workspace w = make_ws(ws, R);
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
     const bool tc = (H % 512 == 0);
+    if (tc && R > kTcFp4Rows) {
+        // CTA-pair kernel: up to 256 rows per pass over the head
+        cudaError_t e = cudaSuccess;
+        for (int r0 = 0; r0 < R && e == cudaSuccess; r0 += kTcRows) {
+            const int nr = std::min(kTcRows, R - r0);
+            vh::AcceptTail tail;
+            if (r0 + nr == R) {
+                tail.draft = draft_ids;
+                tail.next_ids = next_ids;
+                tail.accept_len = accept_len;
+                tail.B = B;
+                tail.k = k;
+            }
+            float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
+            e = vh::launch_verify_fp4_pair(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, V, w, next_ids + r0,
+                                           ml, tail, s);
+            if (e == cudaErrorNotSupported && r0 == 0) break;  // no cluster fits: row groups of 16 below
+        }
+        if (e != cudaErrorNotSupported) return e == cudaSuccess ? VH_OK : launch_status(e);
+        cudaGetLastError();
+    }
     const int grp = tc ? kTcFp4Rows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += grp) {
         const int nr = std::min(grp, R - r0);
