@@ -492,7 +492,7 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
     dX = torch.from_numpy(X.view(np.int16)).to(dev)
     d = torch.from_numpy(synth.corrupt_ids(11, synth.STREAM_CORRUPT, np.zeros((64, 3), np.int32), synth.V_FULL,
                                            1.0)).to(dev)
-    ws = vh.workspace(256)
+    ws = vh.verify_nvfp4_workspace(256, 2048)
     us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(dX, dq, ds, g, d, 64, 3, ws=ws), 10)
     med = statistics.median(us)
     nbytes = q.nbytes + s.nbytes + X.nbytes
@@ -500,7 +500,7 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
     out["full_head_256_rows"] = {
         "workload": "64 seqs x 4 rows x 2048 bf16 vs the full 248,320 x 2048 4-bit head (seed 2; hidden seed 4; "
                     "draft ids uniform, so acceptance is not reported)",
-        "kernel": "k_verify_fp4_pair<256> (CTA pair, exact bf16 dequantisation in shared memory, tcgen05 cta_group::2)",
+        "kernel": "k_hidden_f16 + k_verify_fp4_pair<256> (CTA pair, exact f16 dequantisation in shared memory, tcgen05 cta_group::2)", "gpu_launches_per_round": 2,
         "rounds_per_s": round(1e6 / med, 1), **stats(us),
         "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
         "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
@@ -514,7 +514,7 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
     s = torch.from_numpy(c.s).to(dev)
     X = torch.from_numpy(synth.normal_bf16(7, synth.STREAM_VHIDDEN, (16, 4096), 1.0).view(np.int16)).to(dev)
     d = torch.zeros((4, 3), dtype=torch.int32, device=dev)
-    ws = vh.workspace(16)
+    ws = vh.verify_nvfp4_workspace(16, 4096)
     us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(X, q, s, c.g, d, 4, 3, ws=ws), 20)
     med = statistics.median(us)
     nbytes = c.q.nbytes + c.s.nbytes + 16 * 4096 * 2

@@ -222,23 +222,35 @@ VH_API size_t vh_workspace_error_offset(void);
 VH_API vh_status vh_selftest_bounded_wait(unsigned int* flag, unsigned int timeout_us, void* stream);
 
 /*
+ * Workspace size for spec_verify_greedy_nvfp4 with `rows` = B*(k+1) hidden
+ * rows of width H: the argmax workspace of vh_workspace_bytes(rows) followed
+ * by scratch for f16 copies of the hidden rows (rows*H*2 bytes) and one
+ * float per row, each rounded up to 16 bytes.  0 for rows < 1 or H < 1.
+ */
+VH_API size_t vh_verify_nvfp4_workspace_bytes(int rows, int H);
+
+/*
  * Greedy speculative verification over a block-scaled 4-bit full head (the
  * NVFP4 format of mtp_draft_head_argmax_nvfp4, rows = the V vocabulary
  * entries).  Rows, next_ids, row_maxlogit and accept_len are defined as for
  * spec_verify_greedy, with W_full replaced by the decoded 4-bit head.
  *
- * The head is a quarter of the bf16 head's bytes, so few verified rows
- * (B*(k+1) <= 16 per tensor-core pass) read 4x less memory.  Rows are
- * processed in groups of 16 on the tensor cores (H % 512 == 0) or 8 on CUDA
- * cores (other H); every group reads the head once, so large batches are
- * better served by the bf16 head (spec_verify_greedy), which is
- * tensor-bound at 256 rows either way.
+ * Kernels (H % 512 == 0): up to 16 rows in one tensor-core pass with N = 16;
+ * more rows on a CTA pair (tcgen05 cta_group::2) with N = 128 or 256, up to
+ * 256 rows per pass over the head, after converting the hidden rows to f16
+ * with a per-row power-of-two prescale into the workspace scratch (exact for
+ * every element within 2^31 of its row's largest magnitude).  Other H: CUDA
+ * cores, groups of 8 rows.
  *
  *  hidden        device, bf16 [B*(k+1)][H], 16-byte aligned
  *  Wq, scales    device, uint8 [V][H/2] (32-byte aligned), uint8 [V][H/16] (16-byte aligned)
  *  tensor_scale  finite, > 0
  *  B, k, V       as for spec_verify_greedy;  H: 64 <= H <= 65536, H % 64 == 0
- *  draft_ids, accept_len, next_ids, row_maxlogit, ws: as for spec_verify_greedy
+ *  draft_ids, accept_len, next_ids, row_maxlogit: as for spec_verify_greedy
+ *  ws, ws_bytes  device, 16-byte aligned, zeroed once, at least
+ *                vh_verify_nvfp4_workspace_bytes(B*(k+1), H) bytes
+ *                (VH_ERR_WORKSPACE otherwise); the argmax part is left zeroed,
+ *                the scratch holds the last call's f16 rows
  */
 VH_API vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
                                           float tensor_scale, const int32_t* draft_ids, int B, int k, int H, int V,

@@ -120,6 +120,36 @@ def test_verify_argument_checks(vh):
     assert verify(vh, wsb=vh.vh_workspace_bytes(8) - 1) == vh.VH_ERR_WORKSPACE
 
 
+def verify4(vh, **kw):
+    a = dict(hidden=P, q=P, s=P, g=1.0, d=P, B=8, k=3, H=512, V=4096, acc=P, nid=P, ml=P, ws=P, wsb=None, stream=None)
+    a.update(kw)
+    if a["wsb"] is None:
+        a["wsb"] = vh.vh_verify_nvfp4_workspace_bytes(a["B"] * (a["k"] + 1), a["H"])
+    return vh.lib().spec_verify_greedy_nvfp4(a["hidden"], a["q"], a["s"], a["g"], a["d"], a["B"], a["k"], a["H"],
+                                             a["V"], a["acc"], a["nid"], a["ml"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_verify_nvfp4_workspace_size(vh):
+    # argmax part, then rows*H*2 bytes of f16 rows and 4 bytes per row, each rounded up to 16
+    assert vh.vh_verify_nvfp4_workspace_bytes(0, 512) == 0
+    assert vh.vh_verify_nvfp4_workspace_bytes(4, 0) == 0
+    assert vh.vh_verify_nvfp4_workspace_bytes(256, 2048) == vh.vh_workspace_bytes(256) + 256 * 2048 * 2 + 1024
+    assert vh.vh_verify_nvfp4_workspace_bytes(3, 64) == vh.vh_workspace_bytes(3) + 384 + 16
+    assert vh.vh_verify_nvfp4_workspace_bytes(5, 512) % 16 == 0
+
+
+def test_verify_nvfp4_argument_checks(vh):
+    assert verify4(vh, q=None) == vh.VH_ERR_NULL
+    assert verify4(vh, ws=None) == vh.VH_ERR_NULL
+    assert verify4(vh, H=520) == vh.VH_ERR_SHAPE  # H % 64 != 0
+    assert verify4(vh, k=16) == vh.VH_ERR_SHAPE
+    assert verify4(vh, g=-1.0) == vh.VH_ERR_SHAPE
+    assert verify4(vh, q=P + 16) == vh.VH_ERR_ALIGN
+    # the argmax-only workspace is too small: the f16 scratch is missing
+    assert verify4(vh, wsb=vh.vh_workspace_bytes(32)) == vh.VH_ERR_WORKSPACE
+    assert verify4(vh, wsb=vh.vh_verify_nvfp4_workspace_bytes(32, 512) - 1) == vh.VH_ERR_WORKSPACE
+
+
 def test_valid_call_without_gpu_reports_device(vh):
     import torch
     if torch.cuda.is_available():

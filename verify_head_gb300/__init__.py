@@ -34,7 +34,7 @@ EXPORTS = (
     "vh_version", "vh_status_string", "vh_workspace_bytes", "mtp_draft_head_argmax",
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
     "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather", "vh_workspace_error_offset",
-    "vh_selftest_bounded_wait", "spec_verify_greedy_nvfp4",
+    "vh_selftest_bounded_wait", "spec_verify_greedy_nvfp4", "vh_verify_nvfp4_workspace_bytes",
 )
 
 
@@ -83,6 +83,8 @@ def lib():
         L.mtp_draft_head_argmax_gather.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         L.mtp_draft_head_argmax_static_ws.restype = i32
         L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.vh_verify_nvfp4_workspace_bytes.restype = sz
+        L.vh_verify_nvfp4_workspace_bytes.argtypes = [i32, i32]
         L.spec_verify_greedy_path.restype = i32
         L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
         _lib = L
@@ -95,6 +97,10 @@ def status_string(status: int) -> str:
 
 def vh_workspace_bytes(rows: int) -> int:
     return int(lib().vh_workspace_bytes(int(rows)))
+
+
+def vh_verify_nvfp4_workspace_bytes(rows: int, H: int) -> int:
+    return int(lib().vh_verify_nvfp4_workspace_bytes(int(rows), int(H)))
 
 
 def workspace_error(ws) -> int:
@@ -140,6 +146,12 @@ def workspace(rows: int, device=None):
     """A zeroed workspace for calls producing up to `rows` argmax rows."""
     torch = _torch()
     return torch.zeros(vh_workspace_bytes(rows), dtype=torch.uint8, device=device or "cuda")
+
+
+def verify_nvfp4_workspace(rows: int, H: int, device=None):
+    """A zeroed workspace for spec_verify_greedy_nvfp4 with `rows` hidden rows of width H."""
+    torch = _torch()
+    return torch.zeros(vh_verify_nvfp4_workspace_bytes(rows, H), dtype=torch.uint8, device=device or "cuda")
 
 
 def mtp_draft_head_argmax(hidden, W_cand, cand_ids, ids=None, maxlogit=None, ws=None, stream=None):
@@ -249,7 +261,7 @@ def spec_verify_greedy_nvfp4(hidden, Wq, scales, tensor_scale, draft_ids, B: int
     if row_maxlogit is None and want_maxlogit:
         row_maxlogit = torch.empty(R, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = workspace(R, dev)
+        ws = verify_nvfp4_workspace(R, H, dev)
     st = lib().spec_verify_greedy_nvfp4(_ptr(hidden), _ptr(Wq), _ptr(scales), float(tensor_scale), _ptr(draft_ids), B,
                                         k, H, V, _ptr(accept_len), _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws),
                                         ws.numel(), _stream_ptr(stream))

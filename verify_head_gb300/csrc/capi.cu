@@ -75,6 +75,12 @@ size_t vh_workspace_bytes(int rows) {
     return vh::ws_total_bytes(rows);
 }
 
+size_t vh_verify_nvfp4_workspace_bytes(int rows, int H) {
+    if (rows < 1 || H < 1) return 0;
+    // argmax workspace, then the f16 hidden rows and one float per row
+    return vh::ws_total_bytes(rows) + vh::round16((size_t)rows * (size_t)H * 2) + vh::round16((size_t)rows * 4);
+}
+
 vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const int32_t* cand_ids, int B, int H,
                                 int Vc, int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
     if (!hidden || !W_cand || !cand_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
@@ -207,7 +213,7 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
         !aligned(accept_len, 4) || !aligned(next_ids, 4) || !aligned(row_maxlogit, 4) || !aligned(ws, 16))
         return VH_ERR_ALIGN;
     const int R = B * (k + 1);
-    if (ws_bytes < vh_workspace_bytes(R)) return VH_ERR_WORKSPACE;
+    if (ws_bytes < vh_verify_nvfp4_workspace_bytes(R, H)) return VH_ERR_WORKSPACE;
     vh_status st = check_device();
     if (st != VH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -215,8 +221,12 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
     const bool tc = (H % 512 == 0);
     if (tc && R > kTcFp4Rows) {
-        // CTA-pair kernel: up to 256 rows per pass over the head
-        cudaError_t e = cudaSuccess;
+        // CTA-pair kernel over f16 copies of the hidden rows (workspace), up to
+        // 256 rows per pass over the head
+        uint16_t* xh = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + vh::ws_total_bytes(R));
+        float* colscale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xh) + vh::round16((size_t)R * H * 2));
+        cudaError_t e = vh::launch_hidden_f16(x, R, H, tensor_scale, xh, colscale, s);
+        if (e != cudaSuccess) return launch_status(e);
         for (int r0 = 0; r0 < R && e == cudaSuccess; r0 += kTcRows) {
             const int nr = std::min(kTcRows, R - r0);
             vh::AcceptTail tail;
@@ -228,8 +238,8 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
                 tail.k = k;
             }
             float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
-            e = vh::launch_verify_fp4_pair(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, V, w, next_ids + r0,
-                                           ml, tail, s);
+            e = vh::launch_verify_fp4_pair(xh + (size_t)r0 * H, colscale + r0, nr, H, Wq, scales, V, w,
+                                           next_ids + r0, ml, tail, s);
             if (e == cudaErrorNotSupported && r0 == 0) break;  // no cluster fits: row groups of 16 below
         }
         if (e != cudaErrorNotSupported) return e == cudaSuccess ? VH_OK : launch_status(e);

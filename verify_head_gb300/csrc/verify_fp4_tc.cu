@@ -1,5 +1,5 @@
 // Greedy verification over a block-scaled 4-bit full head on a CTA pair
-// (tcgen05 cta_group::2): exact bf16 dequantisation in shared memory feeding
+// (tcgen05 cta_group::2): exact f16 dequantisation in shared memory feeding
 // one M = 256 x N = 256 MMA stream, fused with the per-hidden-row argmax and
 // the accepted-prefix scan.
 //
@@ -10,11 +10,14 @@
 // low nibble), one E4M3 scale per 16 elements along H, one fp32 tensor scale g.
 //
 // Exactness.  Every E2M1 x E4M3 product has at most 6 significant bits and
-// lies in [2^-10, 2688], so it is a bf16 value: the dequantised weight
-// w / g = e2m1 * e4m3 is exact in bf16 and multiplies the caller's bf16
-// hidden rows unchanged.  The product is formed as (e2m1 * 2^-112) *
-// (e4m3 * 2^112) in bf16 arithmetic, both factors and the result normal
-// numbers; the score is the fp32 MMA sum times g.
+// lies in [2^-10, 2688], so it is an f16 value: the dequantised weight
+// w / g = e2m1 * e4m3 is exact in f16 (one cvt.rn.f16x2.e2m1x2 and one f16x2
+// multiply per two weights).  The hidden rows are converted once per call to
+// f16 with a per-row power-of-two prescale 2^k_r (largest |x| into
+// [2^14, 2^15)), exact for every element within 2^31 of the row's largest;
+// the MMA accumulates in fp32 and the score of hidden row r is
+// acc * g * 2^-k_r, applied to each column's winning value (a positive
+// per-column factor does not move the argmax over W rows).
 //
 // Mapping.  A cluster of two CTAs walks 256-row tiles of the head (128 rows
 // per CTA, tile pt, pt + pairs, ...).  Each CTA holds half of the hidden
@@ -23,14 +26,19 @@
 // hidden rows, K = 16), and each CTA's TMEM receives the accumulator rows of
 // its own 128 W rows.
 //
+// Before the pair kernel, k_hidden_f16 (one CTA per hidden row) writes the
+// prescaled f16 rows and the per-row factors g * 2^-k_r into the caller's
+// workspace; the pair kernel is a programmatic dependent launch, so its
+// prologue and its first code loads overlap the conversion.
+//
 // Warp roles (480 threads per CTA):
-//   warp 0       hidden-row producer: TMA of this CTA's half of the hidden
+//   warp 0       hidden-row producer: TMA of this CTA's half of the f16 hidden
 //                rows, K = 64 per stage, completing on the leader's barrier
 //   warp 1       TMEM owner; in the leader, the MMA issuer
 //   warps 2..5   epilogue: TMEM -> per-column (hidden row) argmax
 //   warp 6       code producer: TMA of the codes (256 contiguous bytes per row,
 //                128-byte swizzled) and the scales, K = 512 per raw stage
-//   warps 7..14  dequantisers: raw codes -> bf16 A tile in the 128-byte
+//   warps 7..14  dequantisers: raw codes -> f16 A tile in the 128-byte
 //                swizzled K-major layout of the MMA, K = 64 per A stage
 // Every wait is bounded (vh_ptx.cuh); on expiry the waiting thread raises the
 // workspace error word and the CTA drains its copies, frees TMEM and returns.
@@ -63,6 +71,9 @@ constexpr int kRawBytes = kRawCodes + kRawScales;
 constexpr int kDeqWarps = 8;
 constexpr int kDeqWarp0 = 7;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 480
+constexpr int kTPR = kDeqWarps * 32 / kM;  // dequantiser threads per W row (2 or 4)
+constexpr int kWords = 8 / kTPR;           // code words (8 weights each) per thread per A stage
+static_assert(kTPR == 2 || kTPR == 4, "dequantiser split");
 constexpr int kTmemCols = 512;             // two accumulators of up to 256 columns
 
 template <int N>
@@ -93,7 +104,7 @@ struct Args {
     int H;
     int V;
     int n_ptiles; // ceil(V / 256)
-    float g;
+    const float* colscale;  // [R]: g * 2^-k_r of hidden row r
     Workspace ws;
     unsigned int* err;
     int32_t* next_ids;
@@ -121,6 +132,15 @@ __device__ __forceinline__ void cluster_sync() {
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive on the leader's A-stage barrier with the default (CTA-scope release)
+// semantics.  The dequantised rows a CTA writes are read only by its own SM's
+// tensor core (each CTA of the pair supplies its 128 rows of A); the writer's
+// fence.proxy.async orders them for that reader.  A cluster-scope release
+// here costs a cluster-wide fence per stage and halves the kernel's speed.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // try_wait with cluster-scope acquire: the phase may have been completed by
@@ -188,10 +208,13 @@ __device__ __forceinline__ unsigned long long desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// kind::f16 instruction descriptor: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// kind::f16 instruction descriptor: f16 A and B (format 0), fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_pair(uint32_t tmem_d, unsigned long long adesc, unsigned long long bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -213,19 +236,16 @@ __device__ __forceinline__ void commit_pair(unsigned long long* bar) {
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ float redux_max_f32(float x) {
@@ -234,19 +254,22 @@ __device__ __forceinline__ float redux_max_f32(float x) {
     return r;
 }
 
-// Column argmax over a warp's 32 W rows for 32 hidden columns (see verify_tc.cu).
-__device__ __forceinline__ void column_argmax32(const float (&v)[32], bool valid, float& m_out, uint32_t& b_out) {
+// Column argmax over a warp's 32 W rows for 16 hidden columns: v[j] is this
+// lane's (W row's) score for column j.  Per column one redux gives the warp
+// maximum and one ballot the lanes reaching it; a 4-level select tree hands
+// column (lane % 16) to this lane: returns its maximum and ballot.
+__device__ __forceinline__ void column_argmax16(const float (&v)[16], bool valid, float& m_out, uint32_t& b_out) {
     const int lane = threadIdx.x & 31;
-    float m[32];
-    uint32_t b[32];
+    float m[16];
+    uint32_t b[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < 16; ++j) {
         const float x = valid ? v[j] : -__int_as_float(0x7f800000);
         m[j] = redux_max_f32(x);
         b[j] = __ballot_sync(0xFFFFFFFFu, valid && x == m[j]);
     }
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
+    for (int s = 8; s >= 1; s >>= 1) {
         const bool hi = (lane & s) != 0;
 #pragma unroll
         for (int i = 0; i < s; ++i) {
@@ -280,41 +303,26 @@ __device__ __forceinline__ uint32_t e2m1_h2(uint32_t word) {
     return h2;
 }
 
-// f16x2 of E2M1 values (normal or zero, mantissa bits 0..8 clear) -> bf16x2
-// of the same values times 2^-112: dropping three mantissa bits moves the
-// 5-bit f16 exponent field into the low bits of the 8-bit bf16 field (bias
-// 15 read as bias 127); the signs stay in place.
-__device__ __forceinline__ uint32_t h2_to_bf2_scaled(uint32_t h) {
-    return ((h & 0x7FFF7FFFu) >> 3) | (h & 0x80008000u);
-}
-
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
-// Two E4M3 scales (low byte first) -> bf16x2 of scale * 2^112.
-__device__ __forceinline__ uint32_t e4m3x2_bf2_up(uint32_t two) {
+// Two E4M3 scales (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t two) {
     uint32_t h2;
     asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two));
-    float lo, hi;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
-    lo *= 0x1p112f;
-    hi *= 0x1p112f;
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
-    return r;
+    return h2;
 }
 
-// One code word (8 E2M1 weights of one 16-element block) times its bf16 scale
-// pair (the block scale in both halves) -> 4 bf16x2 words, in element order.
+// One code word (8 E2M1 weights of one 16-element block) times its f16 scale
+// pair (the block scale in both halves) -> 4 f16x2 words, in element order.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sc, uint32_t (&o)[4]) {
-    o[0] = bmul2(h2_to_bf2_scaled(e2m1_h2<0>(w)), sc);
-    o[1] = bmul2(h2_to_bf2_scaled(e2m1_h2<1>(w)), sc);
-    o[2] = bmul2(h2_to_bf2_scaled(e2m1_h2<2>(w)), sc);
-    o[3] = bmul2(h2_to_bf2_scaled(e2m1_h2<3>(w)), sc);
+    o[0] = hmul2(e2m1_h2<0>(w), sc);
+    o[1] = hmul2(e2m1_h2<1>(w), sc);
+    o[2] = hmul2(e2m1_h2<2>(w), sc);
+    o[3] = hmul2(e2m1_h2<3>(w), sc);
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, const uint32_t (&v)[4]) {
@@ -324,6 +332,12 @@ __device__ __forceinline__ void sts128(uint32_t addr, const uint32_t (&v)[4]) {
 
 __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&v)[4]) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&v)[4]) { lds128(addr, v); }
+
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&v)[2]) {
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
 }
 
 // ---------------------------------------------------------------------------
@@ -384,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- hidden-row producer (both CTAs) ----------------
         if (lane == 0) {
+            pdl_wait();  // the f16 hidden rows come from the conversion kernel
             const unsigned long long pol_x = policy_evict_last();
             uint32_t it = 0;
             bool ok = true;
@@ -405,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer (leader only) ----------------
         if (lane == 0 && leader) {
-            const uint32_t idesc = idesc_bf16(kPairM, N);
+            const uint32_t idesc = idesc_f16(kPairM, N);
             uint32_t it = 0, local = 0;
             bool ok = true;
             for (int pt = pair; pt < a.n_ptiles && ok; pt += n_pairs, ++local) {
@@ -448,7 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t empty_leader0 = map_to_rank(smem_u32(&bars->tmem_empty[0]), 0);
         const uint32_t empty_leader1 = map_to_rank(smem_u32(&bars->tmem_empty[1]), 0);
-        const float g_scale = a.g;
         uint32_t local = 0;
         for (int pt = pair; pt < a.n_ptiles; pt += n_pairs, ++local) {
             const uint32_t buf = local & 1u;
@@ -457,28 +471,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t row0 = (uint32_t)(pt * kPairM + (int)rank * kM + quarter * 32);
             const bool valid = (int)(row0 + lane) < a.V;
 #pragma unroll
-            for (int g = 0; g < kG; ++g) {
-                float v[32];
-                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 256u + g * 32u, v);
-                if (g + 1 == kG) {
-                    tc_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(buf ? empty_leader1 : empty_leader0);
-                }
+            for (int g = 0; g < kG; ++g) {  // columns 32 g .. 32 g + 31, in two halves; lane l keeps column 32 g + l
+                float m = 0.f;
+                uint32_t bal = 0u;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= g_scale;
-                float m;
-                uint32_t bal;
-                column_argmax32(v, valid, m, bal);
+                for (int hf = 0; hf < 2; ++hf) {
+                    float v[16];
+                    tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 256u + g * 32u + hf * 16u, v);
+                    if (g + 1 == kG && hf == 1) {
+                        tc_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(buf ? empty_leader1 : empty_leader0);
+                    }
+                    float mh;
+                    uint32_t bh;
+                    column_argmax16(v, valid, mh, bh);
+                    if ((lane >> 4) == hf) {
+                        m = mh;
+                        bal = bh;
+                    }
+                }
                 if (bal != 0u && (best_g[g] == 0xFFFFFFFFu || m > best_v[g])) {
                     best_v[g] = m;
                     best_g[g] = row0 + (uint32_t)(__ffs(bal) - 1);
                 }
             }
         }
+        pdl_wait();  // the per-row factors come from the conversion kernel
 #pragma unroll
-        for (int g = 0; g < kG; ++g)
-            if (best_g[g] != 0xFFFFFFFFu) atomicMax(&merge[g * 32 + lane], make_key(best_v[g], best_g[g]));
+        for (int g = 0; g < kG; ++g) {
+            const int col = g * 32 + lane;
+            if (best_g[g] != 0xFFFFFFFFu && col < a.R)
+                atomicMax(&merge[col], make_key(best_v[g] * __ldg(a.colscale + col), best_g[g]));
+        }
     } else if (warp == 6) {
         // ---------------- code producer (each CTA, local barriers) ----------------
         if (lane == 0) {
@@ -501,13 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain(&bars->raw_full[j % kRawStages], (j / kRawStages) & 1u);
         }
     } else {
-        // ---------------- dequantisers (warps 7..14) ----------------
-        // Thread t owns W row t/2 and half (t & 1) of each K = 64 slice: 16
-        // code bytes (two 16-element blocks) -> four 16-byte chunks of the
-        // bf16 A tile.  The A tile is K-major with a 128-byte swizzle: row r
-        // at (r / 8) * 1024 + (r % 8) * 128, chunk c at 16 * (c ^ (r % 8)).
-        const int t = threadIdx.x - kDeqWarp0 * 32;  // 0..255
-        const int row = t >> 1, half = t & 1;
+        // ---------------- dequantisers (warps 7..) ----------------
+        // kTPR threads share a W row; thread `part` of a row owns 32 / kTPR
+        // consecutive weights of each K = 64 slice: 4 kWords code bytes ->
+        // kWords 16-byte chunks of the bf16 A tile.  The A tile is K-major
+        // with a 128-byte swizzle: row r at (r / 8) * 1024 + (r % 8) * 128,
+        // chunk c at 16 * (c ^ (r % 8)).
+        const int t = threadIdx.x - kDeqWarp0 * 32;
+        const int row = t / kTPR, part = t % kTPR;
         const uint32_t a_row_off = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
         const uint32_t a_full_addr0 = leader ? 0u : map_to_rank(smem_u32(&bars->a_full[0]), 0);
         uint32_t rit = 0, ait = 0;
@@ -532,20 +558,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < kAPerRaw; ++j, ++ait) {
                     const int as = ait % kAStages;
                     if (!mbar_wait(&bars->a_empty[as], ((ait / kAStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
-                    // code bytes 32 j + 16 half .. +15 of this row's 256-byte piece
-                    const int boff = 32 * j + 16 * half;
+                    // code bytes 32 j + 4 kWords part .. of this row's 256-byte piece
+                    const int boff = 32 * j + 4 * kWords * part;
                     const int seg = row * 2 + (boff >> 7);
-                    uint32_t q[4];
-                    lds128(raw + (uint32_t)(seg * 128 + ((((boff >> 4) & 7) ^ (seg & 7)) << 4)), q);
-                    // blocks 4 j + 2 half and + 1: bytes 2 half, 2 half + 1 of scale word j
-                    const uint32_t sp = e4m3x2_bf2_up((sc[j] >> (16 * half)) & 0xFFFFu);
+                    const uint32_t qaddr = raw + (uint32_t)(seg * 128 + ((((boff >> 4) & 7) ^ (seg & 7)) << 4) + (boff & 8));
+                    uint32_t q[kWords];
+                    lds_words(qaddr, q);
+                    // word i belongs to block 4 j + part kWords / 2 + i / 2: that byte of scale word j
+                    const uint32_t sw = sc[j] >> (8 * part * (kWords / 2));
+                    const uint32_t sp = e4m3x2_h2(kWords == 4 ? (sw & 0xFFFFu) : (sw & 0xFFu) * 0x101u);
                     const uint32_t s0 = __byte_perm(sp, 0, 0x1010), s1 = __byte_perm(sp, 0, 0x3232);
                     const uint32_t a_base = smem_u32(a_ring + (size_t)as * kABytes) + a_row_off;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {  // word i = elements 8 i .. 8 i + 7 of the 32
+                    for (int i = 0; i < kWords; ++i) {  // word i = weights 8 i .. 8 i + 7 of this thread's run
                         uint32_t o[4];
                         dequant_word(q[i], i < 2 ? s0 : s1, o);
-                        const int c = 4 * half + i;
+                        const int c = kWords * part + i;
                         sts128(a_base + (uint32_t)((c ^ (row & 7)) << 4), o);
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -554,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (leader)
                             mbar_arrive(&bars->a_full[as]);
                         else
-                            mbar_arrive_cluster(a_full_addr0 + (uint32_t)(as * 8));
+                            mbar_arrive_remote(a_full_addr0 + (uint32_t)(as * 8));
                     }
                 }
                 __syncwarp();
@@ -564,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- pair teardown, publish, last-CTA decode ----------------
+    pdl_wait();  // the workspace keys may still be read by an earlier launch
     tc_before();
     __syncthreads();
     cluster_sync();
@@ -644,7 +673,7 @@ static bool make_map_scales(CUtensorMap* m, const void* base, int rows, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Hidden rows [R][H] bf16, [box_rows][64] box, 128-byte swizzle (rows past R
+// f16 hidden rows [R][H], [box_rows][64] box, 128-byte swizzle (rows past R
 // read as zeros).
 static bool make_map_x(CUtensorMap* m, const void* base, int R, int H, int box_rows) {
     auto enc = get_encode();
@@ -653,7 +682,7 @@ static bool make_map_x(CUtensorMap* m, const void* base, int R, int H, int box_r
     cuuint64_t strides[1] = {(cuuint64_t)H * 2};
     cuuint32_t box[2] = {(cuuint32_t)kKa, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -668,41 +697,100 @@ static cudaError_t launch_pair(const CUtensorMap& map_q, const CUtensorMap& map_
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(sm_count() / 2, a.n_ptiles)));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, k_verify_fp4_pair<N>, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        return cudaErrorNotSupported;
+    static int clusters_cache[2][64] = {};  // per kernel instantiation and device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int& clusters = clusters_cache[N == 256][dev & 63];
+    if (clusters < 1) {
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, k_verify_fp4_pair<N>, &cfg) != cudaSuccess || c < 1) {
+            cudaGetLastError();
+            return cudaErrorNotSupported;
+        }
+        clusters = c;
     }
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(clusters, a.n_ptiles)));
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_verify_fp4_pair<N>, map_q, map_s, map_x, a);
+}
+
+// Hidden rows bf16 [R][H] -> f16 [R][H] times 2^k_r (largest |x| of row r
+// into [2^14, 2^15); k_r = 0 for an all-zero row), and colscale[r] =
+// g * 2^-k_r.  One CTA per row.
+__global__ void __launch_bounds__(256) k_hidden_f16(const uint16_t* __restrict__ X, int H, float g,
+                                                    uint16_t* __restrict__ Xh, float* __restrict__ colscale) {
+    __shared__ float s_max[8];
+    pdl_launch_dependents();
+    pdl_wait();  // X may come from the previous kernel; Xh may still be read by an earlier launch
+    const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(X + (size_t)r * H);
+    float m = 0.f;
+    for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {
+        const uint32_t pr = xr[i];
+        m = fmaxf(m, fmaxf(fabsf(bf_lo(pr)), fabsf(bf_hi(pr))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    m = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w]);
+    const int k = m > 0.f ? min(127, 141 - (int)((__float_as_uint(m) >> 23) & 0xFF)) : 0;
+    const float up = ldexpf(1.f, k);
+    uint32_t* out = reinterpret_cast<uint32_t*>(Xh + (size_t)r * H);
+    for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {
+        const uint32_t pr = xr[i];
+        uint32_t h2;
+        asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(h2) : "f"(bf_lo(pr) * up), "f"(bf_hi(pr) * up));
+        out[i] = h2;
+    }
+    if (threadIdx.x == 0) colscale[r] = g * ldexpf(1.f, -k);
 }
 
 }  // namespace fp4v
 
-cudaError_t launch_verify_fp4_pair(const uint16_t* X, int R, int H, const uint8_t* Wq, const uint8_t* scales, float g,
-                                   int V, Workspace ws, int32_t* next_ids, float* maxlogit, const AcceptTail& tail,
-                                   cudaStream_t s) {
+cudaError_t launch_hidden_f16(const uint16_t* X, int R, int H, float g, uint16_t* Xh, float* colscale, cudaStream_t s) {
+    using namespace fp4v;
+    if (R < 1 || H < 2 || H % 2 != 0) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)R);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_hidden_f16, X, H, g, Xh, colscale);
+}
+
+cudaError_t launch_verify_fp4_pair(const uint16_t* Xh, const float* colscale, int R, int H, const uint8_t* Wq,
+                                   const uint8_t* scales, int V, Workspace ws, int32_t* next_ids, float* maxlogit,
+                                   const AcceptTail& tail, cudaStream_t s) {
     using namespace fp4v;
     if (R < 1 || R > 256 || H < kKs || H % kKs != 0 || V < 1) return cudaErrorNotSupported;  // H % 512 == 0
     const int N = R <= 128 ? 128 : 256;
     alignas(64) CUtensorMap map_q, map_s, map_x;
     if (!make_map_codes(&map_q, Wq, V, H) || !make_map_scales(&map_s, scales, V, H) ||
-        !make_map_x(&map_x, X, R, H, N / 2))
+        !make_map_x(&map_x, Xh, R, H, N / 2))
         return cudaErrorNotSupported;
     Args a{};
     a.R = R;
     a.H = H;
     a.V = V;
     a.n_ptiles = (V + kPairM - 1) / kPairM;
-    a.g = g;
+    a.colscale = colscale;
     a.ws = ws;
     a.err = ws.ticket + 1;
     a.next_ids = next_ids;

@@ -73,6 +73,7 @@ constexpr size_t kWsHeaderBytes = 16;
 constexpr size_t kWsErrorOffset = 4;
 __host__ __device__ constexpr size_t ws_keys_bytes(int rows) { return ((size_t)rows * 8 + 15) / 16 * 16; }
 __host__ __device__ constexpr size_t ws_total_bytes(int rows) { return kWsHeaderBytes + ws_keys_bytes(rows); }
+__host__ __device__ constexpr size_t round16(size_t n) { return (n + 15) / 16 * 16; }
 
 // Views of a workspace base pointer (the row count does not move anything).
 __host__ __device__ inline Workspace ws_view(void* base) {

@@ -45,13 +45,18 @@ cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq,
 cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
                              int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
 
-// Block-scaled 4-bit full head on a CTA pair (exact bf16 dequantisation in
+// bf16 hidden rows [R][H] -> f16 rows prescaled by 2^k_r (largest |x| into
+// [2^14, 2^15)) and colscale[r] = g * 2^-k_r, for launch_verify_fp4_pair.
+cudaError_t launch_hidden_f16(const uint16_t* X, int R, int H, float g, uint16_t* Xh, float* colscale, cudaStream_t s);
+
+// Block-scaled 4-bit full head on a CTA pair (exact f16 dequantisation in
 // shared memory, tcgen05 cta_group::2, M = 256 W rows x N = 128 or 256 hidden
-// rows) + per-row argmax + acceptance scan, R <= 256, H % 512 == 0.  Returns
-// cudaErrorNotSupported for other shapes or when no cluster fits.
-cudaError_t launch_verify_fp4_pair(const uint16_t* X, int R, int H, const uint8_t* Wq, const uint8_t* scales, float g,
-                                   int V, Workspace ws, int32_t* next_ids, float* maxlogit, const AcceptTail& tail,
-                                   cudaStream_t s);
+// rows) + per-row argmax + acceptance scan over the f16 rows of
+// launch_hidden_f16, R <= 256, H % 512 == 0.  Returns cudaErrorNotSupported
+// for other shapes or when no cluster fits.
+cudaError_t launch_verify_fp4_pair(const uint16_t* Xh, const float* colscale, int R, int H, const uint8_t* Wq,
+                                   const uint8_t* scales, int V, Workspace ws, int32_t* next_ids, float* maxlogit,
+                                   const AcceptTail& tail, cudaStream_t s);
 
 int sm_count();
 
