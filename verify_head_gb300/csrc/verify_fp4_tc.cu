@@ -36,10 +36,11 @@
 //                rows, K = 64 per stage, completing on the leader's barrier
 //   warp 1       TMEM owner; in the leader, the MMA issuer
 //   warps 2..5   epilogue: TMEM -> per-column (hidden row) argmax
-//   warp 6       code producer: TMA of the codes (256 contiguous bytes per row,
-//                128-byte swizzled) and the scales, K = 512 per raw stage
-//   warps 7..14  dequantisers: raw codes -> f16 A tile in the 128-byte
-//                swizzled K-major layout of the MMA, K = 64 per A stage
+//   warp 6       code producer: TMA of the codes (128 contiguous bytes per
+//                row, 128-byte swizzled) and the scales, K = 256 per raw stage
+//   warps 7..14  dequantisers: raw codes -> f16 A tile (two 128-byte
+//                swizzled K-major atoms of K = 64), K = 128 per A stage: each
+//                hand-off to the MMA carries 8 MMAs of work
 // Every wait is bounded (vh_ptx.cuh); on expiry the waiting thread raises the
 // workspace error word and the CTA drains its copies, frees TMEM and returns.
 #include <cuda.h>
@@ -58,28 +59,28 @@ using namespace ptx;
 
 constexpr int kM = 128;                    // W rows per CTA per tile
 constexpr int kPairM = 2 * kM;             // W rows per pair tile (MMA M)
-constexpr int kKa = 64;                    // K per A / hidden stage (one 128-byte bf16 swizzle atom)
-constexpr int kKs = 512;                   // K per raw stage (256 code bytes per row)
-constexpr int kAPerRaw = kKs / kKa;        // 8
+constexpr int kKx = 64;                    // K per hidden-row stage (one 128-byte f16 swizzle atom)
+constexpr int kKa = 128;                   // K per A stage (two swizzle atoms of 16 KiB)
+constexpr int kKs = 256;                   // K per raw stage (128 code bytes per row)
+constexpr int kAPerRaw = kKs / kKa;        // 2
 constexpr int kAStages = 3;
-constexpr int kXStages = 5;
-constexpr int kRawStages = 2;
-constexpr int kABytes = kM * kKa * 2;      // 16 KiB
-constexpr int kRawCodes = kM * kKs / 2;    // 32 KiB: [128 rows][2 x 128 B], 128-byte swizzled
-constexpr int kRawScales = kM * kKs / 16;  // 4 KiB: [128 rows][32 B]
+constexpr int kXStages = 4;
+constexpr int kRawStages = 3;
+constexpr int kAAtom = kM * 128;           // 16 KiB: 128 rows x 64 K
+constexpr int kABytes = kAAtom * (kKa / 64);  // 32 KiB
+constexpr int kRawCodes = kM * kKs / 2;    // 16 KiB: [128 rows][128 B], 128-byte swizzled
+constexpr int kRawScales = kM * kKs / 16;  // 2 KiB: [128 rows][16 B]
 constexpr int kRawBytes = kRawCodes + kRawScales;
 constexpr int kDeqWarps = 8;
 constexpr int kDeqWarp0 = 7;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 480
-constexpr int kTPR = kDeqWarps * 32 / kM;  // dequantiser threads per W row (2 or 4)
-constexpr int kWords = 8 / kTPR;           // code words (8 weights each) per thread per A stage
-static_assert(kTPR == 2 || kTPR == 4, "dequantiser split");
 constexpr int kTmemCols = 512;             // two accumulators of up to 256 columns
+static_assert(kRawBytes % 1024 == 0 && kABytes % 1024 == 0, "stage alignment");
 
 template <int N>
 struct Cfg {
     static constexpr int kXRows = N / 2;                // hidden rows per CTA
-    static constexpr int kXBytes = kXRows * kKa * 2;    // per hidden stage
+    static constexpr int kXBytes = kXRows * kKx * 2;    // per hidden stage
     static constexpr size_t kSmem = 1024 + (size_t)kAStages * kABytes + (size_t)kXStages * kXBytes +
                                     (size_t)kRawStages * kRawBytes + 256 /*barriers*/ + 256 * 8 /*merge*/ + 64;
 };
@@ -175,15 +176,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<unsigned long long>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, unsigned long long* bar, int x, int y,
-                                            int z, unsigned long long policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<unsigned long long>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 
@@ -334,11 +326,6 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&v)[4]) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
 }
 
-__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&v)[4]) { lds128(addr, v); }
-
-__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&v)[2]) {
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
-}
 
 // ---------------------------------------------------------------------------
 
@@ -349,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<N>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* raw_ring = smem;                                          // kRawStages x 36 KiB (1024-aligned)
-    uint8_t* a_ring = raw_ring + (size_t)kRawStages * kRawBytes;       // kAStages x 16 KiB
+    uint8_t* raw_ring = smem;                                          // kRawStages x 18 KiB (1024-aligned)
+    uint8_t* a_ring = raw_ring + (size_t)kRawStages * kRawBytes;       // kAStages x 32 KiB
     uint8_t* x_ring = a_ring + (size_t)kAStages * kABytes;             // kXStages x N/2 x 128 B
     Bars* bars = reinterpret_cast<Bars*>(x_ring + (size_t)kXStages * C::kXBytes);
     unsigned long long* merge = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(bars) + 256);
@@ -360,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-    const int k_steps = a.H / kKa, raw_steps = a.H / kKs;
+    const int x_steps = a.H / kKx, a_steps = a.H / kKa, raw_steps = a.H / kKs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
@@ -403,12 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int pt = pair; pt < a.n_ptiles && ok; pt += n_pairs) {
-                for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                for (int ks = 0; ks < x_steps; ++ks, ++it) {
                     const int s = it % kXStages;
                     if (!mbar_wait(&bars->x_empty[s], ((it / kXStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&bars->x_full[s], 2u * (uint32_t)C::kXBytes);
                     tma_load_2d_pair(x_ring + (size_t)s * C::kXBytes, &map_x, map_to_rank(smem_u32(&bars->x_full[s]), 0),
-                                     ks * kKa, (int)rank * C::kXRows, pol_x);
+                                     ks * kKx, (int)rank * C::kXRows, pol_x);
                 }
             }
             if (leader) {
@@ -421,28 +408,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer (leader only) ----------------
         if (lane == 0 && leader) {
             const uint32_t idesc = idesc_f16(kPairM, N);
-            uint32_t it = 0, local = 0;
+            uint32_t ita = 0, itx = 0, local = 0;
             bool ok = true;
             for (int pt = pair; pt < a.n_ptiles && ok; pt += n_pairs, ++local) {
                 const uint32_t buf = local & 1u;
                 if (!mbar_wait(&bars->tmem_empty[buf], ((local >> 1) & 1u) ^ 1u, a.err)) break;
                 tc_after();
                 const uint32_t d_tmem = tmem_base + buf * 256u;
-                for (int ks = 0; ks < k_steps; ++ks, ++it) {
-                    const int xs = it % kXStages, as = it % kAStages;
-                    if (!mbar_wait(&bars->x_full[xs], (it / kXStages) & 1u, a.err) ||
-                        !mbar_wait_cluster(&bars->a_full[as], (it / kAStages) & 1u, a.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_after();
+                for (int ka = 0; ka < a_steps && ok; ++ka, ++ita) {
+                    const int as = ita % kAStages;
+                    if (!mbar_wait_cluster(&bars->a_full[as], (ita / kAStages) & 1u, a.err)) { ok = false; break; }
                     const uint32_t sa = smem_u32(a_ring + (size_t)as * kABytes);
-                    const uint32_t sb = smem_u32(x_ring + (size_t)xs * C::kXBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kKa / 16; ++kk)
-                        mma_pair(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
-                                 (ks > 0 || kk > 0) ? 1u : 0u);
-                    commit_pair(&bars->x_empty[xs]);
+                    for (int xh = 0; xh < kKa / kKx; ++xh, ++itx) {  // one hidden-row stage per A atom
+                        const int xs = itx % kXStages;
+                        if (!mbar_wait(&bars->x_full[xs], (itx / kXStages) & 1u, a.err)) { ok = false; break; }
+                        tc_after();
+                        const uint32_t sb = smem_u32(x_ring + (size_t)xs * C::kXBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kKx / 16; ++kk)
+                            mma_pair(d_tmem, desc_sw128(sa + xh * kAAtom + kk * 32), desc_sw128(sb + kk * 32), idesc,
+                                     (ka > 0 || xh > 0 || kk > 0) ? 1u : 0u);
+                        commit_pair(&bars->x_empty[xs]);
+                    }
+                    if (!ok) break;
                     commit_pair(&bars->a_empty[as]);
                 }
                 if (ok) commit_pair(&bars->tmem_full[buf]);
@@ -517,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(&bars->raw_empty[s], ((it / kRawStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     uint8_t* dst = raw_ring + (size_t)s * kRawBytes;
                     mbar_arrive_expect_tx(&bars->raw_full[s], kRawBytes);
-                    tma_load_3d(dst, &map_q, &bars->raw_full[s], 0, r * (kKs / 256), row, pol);
+                    tma_load_2d(dst, &map_q, &bars->raw_full[s], r * (kKs / 2), row, pol);
                     tma_load_2d(dst + kRawCodes, &map_s, &bars->raw_full[s], r * (kKs / 16), row, pol);
                 }
             }
@@ -526,15 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain(&bars->raw_full[j % kRawStages], (j / kRawStages) & 1u);
         }
     } else {
-        // ---------------- dequantisers (warps 7..) ----------------
-        // kTPR threads share a W row; thread `part` of a row owns 32 / kTPR
-        // consecutive weights of each K = 64 slice: 4 kWords code bytes ->
-        // kWords 16-byte chunks of the bf16 A tile.  The A tile is K-major
-        // with a 128-byte swizzle: row r at (r / 8) * 1024 + (r % 8) * 128,
-        // chunk c at 16 * (c ^ (r % 8)).
-        const int t = threadIdx.x - kDeqWarp0 * 32;
-        const int row = t / kTPR, part = t % kTPR;
-        const uint32_t a_row_off = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+        // ---------------- dequantisers (warps 7..14) ----------------
+        // Warp w covers W rows 16 w .. 16 w + 15: lane l takes row
+        // 16 w + (l % 8) + 8 (l / 16) and half h = (l / 8) % 2 of each K = 128
+        // A stage, i.e. 64 weights = 32 code bytes (two 16-byte units of the
+        // row's 128-byte raw piece) and four block scales, written as eight
+        // 16-byte chunks into swizzle atom h of the A stage.  The 8 lanes of a
+        // quarter-warp hold 8 consecutive rows with one h, so both the
+        // swizzled code loads and the swizzled A stores hit 8 distinct bank
+        // groups.  Row r of an atom sits at (r / 8) * 1024 + (r % 8) * 128,
+        // its chunk c at 16 * (c ^ (r % 8)).
+        const int t = threadIdx.x - kDeqWarp0 * 32;  // 0..255
+        const int wl = t & 31;
+        const int row = 16 * (t >> 5) + (wl & 7) + 8 * (wl >> 4), half = (wl >> 3) & 1;
+        const uint32_t sw7 = (uint32_t)(row & 7);
+        const uint32_t a_row_off = (uint32_t)(half * kAAtom + (row >> 3) * 1024 + (row & 7) * 128);
         const uint32_t a_full_addr0 = leader ? 0u : map_to_rank(smem_u32(&bars->a_full[0]), 0);
         uint32_t rit = 0, ait = 0;
         bool ok = true;
@@ -543,38 +538,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rs = rit % kRawStages;
                 if (!mbar_wait(&bars->raw_full[rs], (rit / kRawStages) & 1u, a.err)) { ok = false; break; }
                 const uint32_t raw = smem_u32(raw_ring + (size_t)rs * kRawBytes);
-                uint32_t sc[8];  // this row's 32 scale bytes of the raw stage
-                {
-                    uint32_t v0[4], v1[4];
-                    lds128(raw + (uint32_t)(kRawCodes + row * 32), v0);
-                    lds128(raw + (uint32_t)(kRawCodes + row * 32 + 16), v1);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        sc[i] = v0[i];
-                        sc[4 + i] = v1[i];
-                    }
-                }
+                uint32_t sc[4];  // this row's 16 scale bytes of the raw stage (blocks 0..15)
+                lds128(raw + (uint32_t)(kRawCodes + row * 16), sc);
 #pragma unroll
                 for (int j = 0; j < kAPerRaw; ++j, ++ait) {
                     const int as = ait % kAStages;
                     if (!mbar_wait(&bars->a_empty[as], ((ait / kAStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
-                    // code bytes 32 j + 4 kWords part .. of this row's 256-byte piece
-                    const int boff = 32 * j + 4 * kWords * part;
-                    const int seg = row * 2 + (boff >> 7);
-                    const uint32_t qaddr = raw + (uint32_t)(seg * 128 + ((((boff >> 4) & 7) ^ (seg & 7)) << 4) + (boff & 8));
-                    uint32_t q[kWords];
-                    lds_words(qaddr, q);
-                    // word i belongs to block 4 j + part kWords / 2 + i / 2: that byte of scale word j
-                    const uint32_t sw = sc[j] >> (8 * part * (kWords / 2));
-                    const uint32_t sp = e4m3x2_h2(kWords == 4 ? (sw & 0xFFFFu) : (sw & 0xFFu) * 0x101u);
-                    const uint32_t s0 = __byte_perm(sp, 0, 0x1010), s1 = __byte_perm(sp, 0, 0x3232);
+                    // code units 4 j + 2 h and 4 j + 2 h + 1 of the row (weights 128 j + 64 h .. + 63)
+                    const uint32_t u0 = (uint32_t)(4 * j + 2 * half);
+                    uint32_t q[8];
+                    {
+                        uint32_t q0[4], q1[4];
+                        lds128(raw + (uint32_t)(row * 128) + (((u0) ^ sw7) << 4), q0);
+                        lds128(raw + (uint32_t)(row * 128) + (((u0 + 1) ^ sw7) << 4), q1);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            q[i] = q0[i];
+                            q[4 + i] = q1[i];
+                        }
+                    }
+                    // blocks 8 j + 4 h .. + 3: scale word 2 j + h
+                    const uint32_t sw = half ? sc[2 * j + 1] : sc[2 * j];
+                    const uint32_t s01 = e4m3x2_h2(sw & 0xFFFFu), s23 = e4m3x2_h2(sw >> 16);
+                    const uint32_t sb[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
+                                            __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
                     const uint32_t a_base = smem_u32(a_ring + (size_t)as * kABytes) + a_row_off;
 #pragma unroll
-                    for (int i = 0; i < kWords; ++i) {  // word i = weights 8 i .. 8 i + 7 of this thread's run
+                    for (int i = 0; i < 8; ++i) {  // word i = weights 8 i .. 8 i + 7 of the 64 = chunk i of the atom row
                         uint32_t o[4];
-                        dequant_word(q[i], i < 2 ? s0 : s1, o);
-                        const int c = kWords * part + i;
-                        sts128(a_base + (uint32_t)((c ^ (row & 7)) << 4), o);
+                        dequant_word(q[i], sb[i >> 1], o);
+                        sts128(a_base + (((uint32_t)i ^ sw7) << 4), o);
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
@@ -646,21 +639,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// Codes [V][H/2] bytes viewed as [V][H/256][128]: a [128 rows][2][128 B] box
-// reads 256 contiguous bytes of every row, stored 128-byte swizzled.
+// Codes [V][H/2] bytes, [128 rows][128 B] box (K = 256), 128-byte swizzle.
 static bool make_map_codes(CUtensorMap* m, const void* base, int rows, int H) {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)(H / 256), (cuuint64_t)rows};
-    cuuint64_t strides[2] = {128, (cuuint64_t)(H / 2)};
-    cuuint32_t box[3] = {128, (cuuint32_t)(kKs / 256), (cuuint32_t)kM};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[2] = {(cuuint64_t)(H / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(H / 2)};
+    cuuint32_t box[2] = {(cuuint32_t)(kKs / 2), (cuuint32_t)kM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scales [V][H/16] bytes, [128 rows][32 B] box, no swizzle.
+// Scales [V][H/16] bytes, [128 rows][16 B] box, no swizzle.
 static bool make_map_scales(CUtensorMap* m, const void* base, int rows, int H) {
     auto enc = get_encode();
     if (!enc) return false;
@@ -680,7 +672,7 @@ static bool make_map_x(CUtensorMap* m, const void* base, int R, int H, int box_r
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)R};
     cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKa, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kKx, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -779,7 +771,7 @@ cudaError_t launch_verify_fp4_pair(const uint16_t* Xh, const float* colscale, in
                                    const uint8_t* scales, int V, Workspace ws, int32_t* next_ids, float* maxlogit,
                                    const AcceptTail& tail, cudaStream_t s) {
     using namespace fp4v;
-    if (R < 1 || R > 256 || H < kKs || H % kKs != 0 || V < 1) return cudaErrorNotSupported;  // H % 512 == 0
+    if (R < 1 || R > 256 || H < kKs || H % kKs != 0 || V < 1) return cudaErrorNotSupported;  // H % 256 == 0
     const int N = R <= 128 ? 128 : 256;
     alignas(64) CUtensorMap map_q, map_s, map_x;
     if (!make_map_codes(&map_q, Wq, V, H) || !make_map_scales(&map_s, scales, V, H) ||
