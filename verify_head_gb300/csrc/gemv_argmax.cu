@@ -37,11 +37,6 @@ struct GemvArgs {
     int H;
     int n_rows;
     int rows_per_warp;
-    // bulk-copy ring kernels only
-    int rows_per_cta;
-    int rows_per_stage;  // multiple of kRingConsumers
-    int stage_bytes;
-    int n_stages;
     unsigned int* err;
     Workspace ws;
     int32_t* ids;
@@ -55,16 +50,6 @@ __device__ __forceinline__ U32x8 ld_x32(const uint16_t* p) {
     U32x8 r;
     r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
     r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
-    return r;
-}
-
-// 32 bytes from shared memory (address in the shared window).
-__device__ __forceinline__ U32x8 lds32(uint32_t saddr) {
-    U32x8 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "r"(saddr));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7]) : "r"(saddr + 16));
     return r;
 }
 
@@ -270,19 +255,10 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two_bytes) {
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy ring geometry (4-bit head, B = 1).
-
-constexpr int kRingConsumers = 8;
-constexpr int kRingThreads = (kRingConsumers + 1) * 32;
-constexpr int kRingMaxStages = 8;
-constexpr int kRingSmem = 192 * 1024;
-
-// ---------------------------------------------------------------------------
-// Block-scaled 4-bit head, B = 1, H <= 8192: bulk-copy ring (codes and scales
-// stream through two shared-memory rings).  Weights decode with one
-// cvt.rn.f16x2.e2m1x2 per byte (exact); the hidden row is held in registers
-// as f16, prescaled by a power of two 2^k so that its largest magnitude
-// lies in [2^14, 2^15) (exact for every element within 2^31 of the largest);
+// Block-scaled 4-bit decode helpers.  Weights decode with one
+// cvt.rn.f16x2.e2m1x2 per byte (exact); the hidden row is held as f16,
+// prescaled by a power of two 2^k so that its largest magnitude lies in
+// [2^14, 2^15) (exact for every element within 2^31 of the largest);
 // products accumulate in fp32 with the mixed-precision fma.rn.f32.f16.  Each
 // 16-element block sum is multiplied by its E4M3 scale; the total by g*2^-k.
 
@@ -294,12 +270,6 @@ __device__ __forceinline__ float fma_f16_f32(unsigned short a, unsigned short b,
     float d;
     asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
     return d;
-}
-
-__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
-    uint32_t h2;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
-    return h2;
 }
 
 // 16-element block: codes in (q0, q1) (element 2i in the low nibble of byte
@@ -354,162 +324,6 @@ __device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
     return r;
 }
 
-template <int CPL>
-__global__ void __launch_bounds__(kRingThreads, 1) k_draft_ring_nvfp4(const GemvArgs a) {
-    extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ __align__(8) unsigned long long full[kRingMaxStages], empty[kRingMaxStages];
-    __shared__ float s_xmax[kRingConsumers];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int H = a.H, nch = H >> 6;  // 64-element chunks: 32 code bytes + 4 scale bytes
-    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
-    const long long row_begin = (long long)blockIdx.x * a.rows_per_cta;
-    const long long row_end = min(row_begin + (long long)a.rows_per_cta, (long long)a.n_rows);
-    const int n_iter = row_end > row_begin ? (int)((row_end - row_begin + a.rows_per_stage - 1) / a.rows_per_stage) : 0;
-    const int S = a.n_stages;
-    const uint32_t qstage = (uint32_t)(a.rows_per_stage * qrow);  // code bytes per stage
-    uint8_t* sring = ring + (size_t)S * qstage;                    // scale ring after the code ring
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], kRingConsumers);
-        }
-        ptx::fence_barrier_init();
-    }
-    // largest |x| (identical in every CTA) -> power-of-two prescale 2^k
-    if (warp < kRingConsumers) {
-        float m = 0.f;
-        for (int i = warp * 32 + lane; i < H; i += kRingConsumers * 32)
-            m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) s_xmax[warp] = m;
-    }
-    __syncthreads();
-
-    unsigned long long best[1] = {0ull};
-    if (warp == kRingConsumers) {
-        if (lane == 0) {
-            const unsigned long long pol = ptx::policy_evict_first();
-            const uint8_t* Wq = static_cast<const uint8_t*>(a.W);
-            int i = 0;
-            for (; i < n_iter; ++i) {
-                const int s = i % S;
-                if (!ptx::mbar_wait(&empty[s], ((i / S) & 1) ^ 1, a.err)) break;
-                const long long r0 = row_begin + (long long)i * a.rows_per_stage;
-                const long long nr = min((long long)a.rows_per_stage, row_end - r0);
-                const uint32_t qb = (uint32_t)(nr * qrow), sb = (uint32_t)(nr * srow);
-                ptx::mbar_arrive_expect_tx(&full[s], qb + sb);
-                ptx::bulk_load(ring + (size_t)s * qstage, Wq + (size_t)r0 * qrow, qb, &full[s], pol);
-                ptx::bulk_load(sring + (size_t)s * a.rows_per_stage * srow, a.scales + (size_t)r0 * srow, sb, &full[s],
-                               pol);
-            }
-            for (int j = (i > S ? i - S : 0); j < i; ++j) ptx::mbar_drain(&full[j % S], (j / S) & 1);
-        }
-    } else {
-        float xmax = 0.f;
-#pragma unroll
-        for (int w = 0; w < kRingConsumers; ++w) xmax = fmaxf(xmax, s_xmax[w]);
-        int k = 0;
-        if (xmax > 0.f) {
-            const int e = (int)((__float_as_uint(xmax) >> 23) & 0xFF);  // biased exponent of the largest |x|
-            k = min(127, 141 - e);                                      // largest |x| * 2^k in [2^14, 2^15)
-        }
-        const float up = ldexpf(1.f, k);
-        const float out_scale = a.g * ldexpf(1.f, -k);
-        uint32_t xh[CPL][32];  // lane's chunks of x as f16x2
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                if (c < nch) {
-                    const uint32_t pr = reinterpret_cast<const uint32_t*>(a.x)[c * 32 + t];
-                    xh[j][t] = f32x2_to_h2(bf_lo(pr) * up, bf_hi(pr) * up);
-                } else {
-                    xh[j][t] = 0u;
-                }
-            }
-        }
-        const uint32_t ring_base = ptx::smem_u32(ring), sring_base = ptx::smem_u32(sring);
-        for (int i = 0; i < n_iter; ++i) {
-            const int s = i % S;
-            if (!ptx::mbar_wait(&full[s], (i / S) & 1, a.err)) break;
-            const long long r0 = row_begin + (long long)i * a.rows_per_stage;
-            float score[4];
-            int nr = 0;
-            for (int rr = warp; rr < a.rows_per_stage && nr < 4; rr += kRingConsumers, ++nr) {
-                float acc = 0.f;
-                if (r0 + rr < row_end) {
-                    const uint32_t qaddr = ring_base + (uint32_t)s * qstage + (uint32_t)(rr * qrow);
-                    const uint32_t saddr = sring_base + (uint32_t)((s * a.rows_per_stage + rr) * srow);
-#pragma unroll
-                    for (int j = 0; j < CPL; ++j) {
-                        const int c = lane + 32 * j;
-                        if (c < nch) {
-                            const U32x8 q = lds32(qaddr + c * 32);
-                            uint32_t sc;
-                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(saddr + c * 4));
-                            const float2 s01 = e4m3x2_to_f2(sc & 0xFFFFu);
-                            const float2 s23 = e4m3x2_to_f2(sc >> 16);
-                            acc = fmaf(nvfp4_block16(q.v[0], q.v[1], &xh[j][0]), s01.x, acc);
-                            acc = fmaf(nvfp4_block16(q.v[2], q.v[3], &xh[j][8]), s01.y, acc);
-                            acc = fmaf(nvfp4_block16(q.v[4], q.v[5], &xh[j][16]), s23.x, acc);
-                            acc = fmaf(nvfp4_block16(q.v[6], q.v[7], &xh[j][24]), s23.y, acc);
-                        }
-                    }
-                }
-                score[nr] = acc;
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty[s]);
-            nr = 0;
-            for (int rr = warp; rr < a.rows_per_stage && nr < 4; rr += kRingConsumers, ++nr) {
-                const long long r = r0 + rr;
-                if (r < row_end) {
-                    const float sc = warp_sum(score[nr]) * out_scale;
-                    const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
-                    const unsigned long long kk = make_key(sc, gid);
-                    best[0] = kk > best[0] ? kk : best[0];
-                }
-            }
-        }
-    }
-    finish_argmax<1, kRingConsumers + 1>(best, a);
-}
-
-static cudaError_t launch_ring_nvfp4(GemvArgs& a, cudaStream_t s) {
-    const int H = a.H;
-    const size_t qrow = (size_t)H / 2, srow = (size_t)H / 16;
-    int rps = (int)std::min<size_t>(32, std::max<size_t>(kRingConsumers, (32768 / qrow) / kRingConsumers *
-                                                                            kRingConsumers));
-    a.rows_per_stage = rps;
-    a.stage_bytes = (int)(rps * (qrow + srow));
-    a.n_stages = std::min(kRingMaxStages, kRingSmem / a.stage_bytes);
-    if (a.n_stages < 2) return cudaErrorNotSupported;
-    const int sms = sm_count();
-    if (sms < 1) return cudaErrorInvalidConfiguration;
-    long long grid = std::min<long long>(sms, ((long long)a.n_rows + rps - 1) / rps);
-    a.rows_per_cta = (int)(((long long)a.n_rows + grid - 1) / grid);
-    grid = ((long long)a.n_rows + a.rows_per_cta - 1) / a.rows_per_cta;
-    const size_t smem = (size_t)a.n_stages * a.stage_bytes;
-    const int cpl = (H / 64 + 31) / 32;
-#define VH_RING4_CASE(C)                                                                                \
-    if (cpl <= C) {                                                                                      \
-        cudaError_t e = cudaFuncSetAttribute(k_draft_ring_nvfp4<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             (int)smem);                                                 \
-        if (e != cudaSuccess) return e;                                                                  \
-        k_draft_ring_nvfp4<C><<<(unsigned)grid, kRingThreads, smem, s>>>(a);                             \
-        return cudaGetLastError();                                                                       \
-    }
-    VH_RING4_CASE(1)
-    VH_RING4_CASE(2)
-    VH_RING4_CASE(4)
-#undef VH_RING4_CASE
-    return cudaErrorNotSupported;
-}
-
-
 // ---------------------------------------------------------------------------
 // Block-scaled 4-bit head, B = 1, H % 64 == 0, H <= 8192: direct streaming.
 // Each warp owns a contiguous run of rows and reads every code row with
@@ -539,7 +353,11 @@ __global__ void __launch_bounds__(kThreads, (CPL >= 4 ? 1 : 2)) k_gemv_nvfp4_dir
 
     // power-of-two prescale from the largest |x| (identical in every CTA)
     float m = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.x)), fabsf(bf_hi(v.x))), fmaxf(fabsf(bf_lo(v.y)), fabsf(bf_hi(v.y)))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.z)), fabsf(bf_hi(v.z))), fmaxf(fabsf(bf_lo(v.w)), fabsf(bf_hi(v.w)))));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) s_xmax[warp] = m;
@@ -645,8 +463,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_gemv_nvfp4_xs(const GemvArgs a)
         for (int c = lane; c < nch; c += 32) prefetch_l2(Wq + (size_t)r * qrow + c * 32);
     pdl_wait();
 
+    // largest |x| over 16-byte pieces (H / 8 of them, one or two per thread)
     float m = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[i] << 16)));
+    const uint4* xv = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+        const uint4 v = __ldg(xv + i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.x)), fabsf(bf_hi(v.x))), fmaxf(fabsf(bf_lo(v.y)), fabsf(bf_hi(v.y)))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.z)), fabsf(bf_hi(v.z))), fmaxf(fabsf(bf_lo(v.w)), fabsf(bf_hi(v.w)))));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) s_xmax[warp] = m;
@@ -656,10 +480,15 @@ __global__ void __launch_bounds__(kThreads, 4) k_gemv_nvfp4_xs(const GemvArgs a)
     for (int w = 0; w < kWarps; ++w) xmax = fmaxf(xmax, s_xmax[w]);
     const int k = xmax > 0.f ? min(127, 141 - (int)((__float_as_uint(xmax) >> 23) & 0xFF)) : 0;
     const float up = ldexpf(1.f, k), out_scale = a.g * ldexpf(1.f, -k);
-    for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {  // word i = elements 2i, 2i+1
-        const uint32_t pr = reinterpret_cast<const uint32_t*>(a.x)[i];
-        const int c = i >> 5, piece = (i >> 2) & 7, w = i & 3;
-        xsh[c * 32 + ((piece ^ (c & 7)) << 2) + w] = f32x2_to_h2(bf_lo(pr) * up, bf_hi(pr) * up);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {  // piece i = elements 8i .. 8i+7
+        const uint4 v = __ldg(xv + i);
+        const int c = i >> 3, piece = i & 7;
+        uint4 h;
+        h.x = f32x2_to_h2(bf_lo(v.x) * up, bf_hi(v.x) * up);
+        h.y = f32x2_to_h2(bf_lo(v.y) * up, bf_hi(v.y) * up);
+        h.z = f32x2_to_h2(bf_lo(v.z) * up, bf_hi(v.z) * up);
+        h.w = f32x2_to_h2(bf_lo(v.w) * up, bf_hi(v.w) * up);
+        *reinterpret_cast<uint4*>(xsh + c * 32 + ((piece ^ (c & 7)) << 2)) = h;
     }
     __syncthreads();
     const uint32_t xbase = ptx::smem_u32(xsh);

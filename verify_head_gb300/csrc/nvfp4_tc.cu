@@ -181,10 +181,13 @@ __device__ __forceinline__ float redux_max_f32(float x) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) {
-    uint32_t h2;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
-    return h2;
+// Four E2M1 pairs (the bytes of `w`, low byte first) -> four f16x2 words,
+// the bytes taken through .b8 register views (no shifts or masks).
+__device__ __forceinline__ void e2m1x8_h2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t two) {
@@ -253,16 +256,22 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     pdl_wait();  // the hidden rows and the workspace may come from the previous kernel
-    // per-row power-of-two prescale of the hidden rows (identical in every CTA)
-    if (warp >= 6) {
-        const int t = threadIdx.x - 6 * 32;  // 0..255: row b = t / 16, 16 threads per row
-        const int b = t >> 4;
+    // per-row power-of-two prescale of the hidden rows (identical in every CTA):
+    // warp w takes rows w, w + 14, ..., each lane 16-byte pieces of the row,
+    // all loads of a row independent
+    for (int b = warp; b < kN; b += kThreadsFp4 / 32) {
         float m = 0.f;
-        if (b < a.nb)
-            for (int i = (t & 15); i < H; i += 16) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)a.x[(size_t)b * H + i] << 16)));
+        if (b < a.nb) {
+            const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)b * H);
+            for (int i = lane; i < H / 8; i += 32) {
+                const uint4 v = __ldg(xr + i);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.x)), fabsf(bf_hi(v.x))), fmaxf(fabsf(bf_lo(v.y)), fabsf(bf_hi(v.y)))));
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(bf_lo(v.z)), fabsf(bf_hi(v.z))), fmaxf(fabsf(bf_lo(v.w)), fabsf(bf_hi(v.w)))));
+            }
+        }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if ((t & 15) == 0) {
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) {
             int k = 0;
             if (m > 0.f) k = min(127, 141 - (int)((__float_as_uint(m) >> 23) & 0xFF));
             s_up[b] = ldexpf(1.f, k);
@@ -433,10 +442,12 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
                         for (int j = 0; j < 4; ++j) {  // word j = elements 8j .. 8j+7 of the chunk
                             const uint32_t ss = j < 2 ? slo : shi;
                             const uint32_t w = q[j];
-                            out[cc * 16 + j * 4 + 0] = hmul2(e2m1x2_h2(w & 0xFFu), ss);
-                            out[cc * 16 + j * 4 + 1] = hmul2(e2m1x2_h2((w >> 8) & 0xFFu), ss);
-                            out[cc * 16 + j * 4 + 2] = hmul2(e2m1x2_h2((w >> 16) & 0xFFu), ss);
-                            out[cc * 16 + j * 4 + 3] = hmul2(e2m1x2_h2(w >> 24), ss);
+                            uint32_t h[4];
+                            e2m1x8_h2(w, h);
+                            out[cc * 16 + j * 4 + 0] = hmul2(h[0], ss);
+                            out[cc * 16 + j * 4 + 1] = hmul2(h[1], ss);
+                            out[cc * 16 + j * 4 + 2] = hmul2(h[2], ss);
+                            out[cc * 16 + j * 4 + 3] = hmul2(h[3], ss);
                         }
                     }
                     tmem_st32(tmem_row + (uint32_t)(as * kACols), out);
