@@ -21,8 +21,8 @@
 //   warps 2..5   epilogue: TMEM -> per-column (hidden row) argmax
 //   warps 6..13  dequantisers: raw codes (128-byte swizzled by TMA) -> f16
 //                A tile in TMEM (tcgen05.st; the MMA reads A from TMEM) and
-//                bf16 hidden slice -> f16 B tile in shared memory, K = 128 per
-//                A/B stage (four per raw stage), 3-deep ring
+//                bf16 hidden slice -> f16 B tile in shared memory, K = 256 per
+//                A/B stage (two per raw stage), 3-deep ring
 // Scores never leave the SM; per-CTA maxima go out as packed-key atomicMax
 // and the last CTA decodes ids.  Waits are bounded (see vh_ptx.cuh).
 #include <cuda.h>
@@ -41,7 +41,7 @@ using namespace ptx;
 
 constexpr int kM = 128;          // weight rows per tile
 constexpr int kKs = 512;         // K per raw (TMA) stage: 256 contiguous code bytes per row
-constexpr int kKa = 128;         // K per dequantised A/B stage (four per raw stage)
+constexpr int kKa = 256;         // K per dequantised A/B stage (two per raw stage)
 constexpr int kAbPerRaw = kKs / kKa;
 constexpr int kN = 16;           // hidden rows per launch (MMA N)
 constexpr int kRawStages = 3;
@@ -51,13 +51,13 @@ constexpr int kRawScales = kM * kKs / 16;  // 4 KiB: [128 rows][32 B]
 constexpr int kXBox = 256;                 // hidden elements per TMA box (box dims are <= 256)
 constexpr int kRawX = kN * kKs * 2;        // 16 KiB: bf16 hidden slice, two [16 rows][256] boxes
 constexpr int kRawBytes = kRawCodes + kRawScales + kRawX;
-constexpr int kBBytes = kN * kKa * 2;      // 4 KiB: 2 atoms of [16 rows x 128 B]
+constexpr int kBBytes = kN * kKa * 2;      // 8 KiB: 4 atoms of [16 rows x 128 B]
 constexpr int kAtomB = kN * 128;           // 2 KiB
 constexpr int kACols = kKa / 2;            // TMEM columns of one A stage (two f16 per column)
 constexpr int kDeqWarps = 8;
 constexpr int kThreadsFp4 = (2 + 4 + kDeqWarps) * 32;  // 448
 constexpr int kAcc = 4;          // independent accumulators per tile (K-steps rotate over them)
-constexpr int kTmemCols = 512;   // A stages at columns 0, 64, 128; accumulators from column 192
+constexpr int kTmemCols = 512;   // A stages at columns 0, 128, 256; accumulators from column 384
 constexpr int kDCol = kAbStages * kACols;
 constexpr int kDBuf = kAcc * kN; // columns per accumulator buffer (two buffers)
 
@@ -395,20 +395,20 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
         }
     } else {
         // ---------------- dequantisers (warps 6..13) ----------------
-        // Each raw stage (K = 256: eight 16-byte code chunks of 32 weights per
-        // row) becomes two A/B stages (K = 128).  The A stage lives in TMEM
-        // (lane = weight row, two f16 of K per column), written straight from
-        // registers with tcgen05.st; a warp may only reach its TMEM lane
-        // quarter (warp % 4), so warps 6..9 write columns 0..31 of the stage
-        // (K 0..63) for their quarter and warps 10..13 columns 32..63.  The
+        // Each raw stage (K = 512: sixteen 16-byte code chunks of 32 weights
+        // per row) becomes two A/B stages (K = 256).  The A stage lives in
+        // TMEM (lane = weight row, two f16 of K per column), written straight
+        // from registers with tcgen05.st; a warp may only reach its TMEM lane
+        // quarter (warp % 4), so warps 6..9 write columns 0..63 of the stage
+        // (K 0..127) for their quarter and warps 10..13 columns 64..127.  The
         // raw codes were stored 128-byte swizzled by the TMA, so the 16-byte
         // loads of 32 consecutive rows are bank-conflict free.
         const int t = threadIdx.x - 6 * 32;  // 0..255
         const int quarter = warp & 3, khalf = (warp - 6) >> 2;
         const int row = quarter * 32 + lane;
-        const int xb = t >> 4, xp = t & 15;  // B row / 8-element part of the hidden slice
+        const int xb = t >> 4, xp = t & 15;  // B row / 16-element part of the hidden slice
         const float up = s_up[xb];
-        const uint32_t tmem_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(khalf * 32);
+        const uint32_t tmem_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(khalf * (kACols / 2));
         uint32_t rit = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < a.n_tiles && ok; tile += gridDim.x) {
@@ -421,45 +421,50 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
                     const int as = abit % kAbStages;
                     if (!mbar_wait(&bars->ab_empty[as], ((abit / kAbStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     tc_after();
-                    const int c0 = h * 4 + khalf * 2;  // first 16-byte code chunk (of 16 in the raw row)
-                    uint32_t sc4;                      // scales of blocks 2*c0 .. 2*c0+3
-                    asm volatile("ld.shared.u32 %0, [%1];"
-                                 : "=r"(sc4)
+                    const int c0 = h * 8 + khalf * 4;  // first 16-byte code chunk (of 16 in the raw row)
+                    uint32_t sc8[2];                   // scales of blocks 2*c0 .. 2*c0+7
+                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                                 : "=r"(sc8[0]), "=r"(sc8[1])
                                  : "r"(raw + (uint32_t)(kRawCodes + row * (kKs / 16) + 2 * c0)));
-                    const uint32_t s01 = e4m3x2_h2(sc4 & 0xFFFFu), s23 = e4m3x2_h2(sc4 >> 16);
-                    uint32_t out[32];
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = c0 + cc;
-                        const int seg = row * 2 + (c >> 3);  // 128-byte segment of the swizzled raw tile
-                        uint32_t q[4];
-                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                     : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
-                                     : "r"(raw + (uint32_t)(seg * 128 + (((c & 7) ^ (seg & 7)) * 16))));
-                        const uint32_t sp = cc ? s23 : s01;
-                        const uint32_t slo = __byte_perm(sp, 0, 0x1010), shi = __byte_perm(sp, 0, 0x3232);
+                    for (int half = 0; half < 2; ++half) {  // 64 weights -> 32 TMEM columns each
+                        const uint32_t sc4 = sc8[half];
+                        const uint32_t s01 = e4m3x2_h2(sc4 & 0xFFFFu), s23 = e4m3x2_h2(sc4 >> 16);
+                        uint32_t out[32];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {  // word j = elements 8j .. 8j+7 of the chunk
-                            const uint32_t ss = j < 2 ? slo : shi;
-                            const uint32_t w = q[j];
-                            uint32_t h[4];
-                            e2m1x8_h2(w, h);
-                            out[cc * 16 + j * 4 + 0] = hmul2(h[0], ss);
-                            out[cc * 16 + j * 4 + 1] = hmul2(h[1], ss);
-                            out[cc * 16 + j * 4 + 2] = hmul2(h[2], ss);
-                            out[cc * 16 + j * 4 + 3] = hmul2(h[3], ss);
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = c0 + 2 * half + cc;
+                            const int seg = row * 2 + (c >> 3);  // 128-byte segment of the swizzled raw tile
+                            uint32_t q[4];
+                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+                                         : "r"(raw + (uint32_t)(seg * 128 + (((c & 7) ^ (seg & 7)) * 16))));
+                            const uint32_t sp = cc ? s23 : s01;
+                            const uint32_t slo = __byte_perm(sp, 0, 0x1010), shi = __byte_perm(sp, 0, 0x3232);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {  // word j = elements 8j .. 8j+7 of the chunk
+                                const uint32_t ss = j < 2 ? slo : shi;
+                                uint32_t hh[4];
+                                e2m1x8_h2(q[j], hh);
+                                out[cc * 16 + j * 4 + 0] = hmul2(hh[0], ss);
+                                out[cc * 16 + j * 4 + 1] = hmul2(hh[1], ss);
+                                out[cc * 16 + j * 4 + 2] = hmul2(hh[2], ss);
+                                out[cc * 16 + j * 4 + 3] = hmul2(hh[3], ss);
+                            }
                         }
+                        tmem_st32(tmem_row + (uint32_t)(as * kACols + half * 32), out);
                     }
-                    tmem_st32(tmem_row + (uint32_t)(as * kACols), out);
-                    {  // hidden slice [16][128] bf16 -> f16 B tile (rows >= nb arrive as zeros)
-                        const int kx = h * kKa + xp * 8;  // element within the raw stage
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {  // hidden slice [16][256] bf16 -> f16 B tile (rows >= nb are zeros)
+                        const int kx = h * kKa + xp * 16 + e * 8;  // element within the raw stage
                         const uint32_t src = raw + (uint32_t)(kRawCodes + kRawScales + (kx / kXBox) * (kN * kXBox * 2) +
                                                               xb * (kXBox * 2) + (kx % kXBox) * 2);
                         uint32_t pr[4];
                         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                                      : "=r"(pr[0]), "=r"(pr[1]), "=r"(pr[2]), "=r"(pr[3]) : "r"(src));
-                        const uint32_t b_addr = smem_u32(b_ring + (size_t)as * kBBytes) + (uint32_t)(xp >> 3) * kAtomB +
-                                                (uint32_t)xb * 128u + (uint32_t)(((xp & 7) ^ (xb & 7)) * 16);
+                        const int piece = 2 * xp + e;  // 8-element piece of the stage (4 atoms of 8)
+                        const uint32_t b_addr = smem_u32(b_ring + (size_t)as * kBBytes) + (uint32_t)(piece >> 3) * kAtomB +
+                                                (uint32_t)xb * 128u + (uint32_t)(((piece & 7) ^ (xb & 7)) * 16);
                         sts128(b_addr, f32x2_h2(bf_lo(pr[0]) * up, bf_hi(pr[0]) * up),
                                f32x2_h2(bf_lo(pr[1]) * up, bf_hi(pr[1]) * up),
                                f32x2_h2(bf_lo(pr[2]) * up, bf_hi(pr[2]) * up),
