@@ -56,6 +56,9 @@ constexpr int kAtomB = kN * 128;           // 2 KiB
 constexpr int kACols = kKa / 2;            // TMEM columns of one A stage (two f16 per column)
 constexpr int kDeqWarps = 8;
 constexpr int kThreadsFp4 = (2 + 4 + kDeqWarps) * 32;  // 448
+constexpr int kKParts = kDeqWarps / 4;  // dequantiser warps per TMEM lane quarter (each a K range)
+constexpr int kPartCols = kACols / kKParts;  // TMEM columns of an A stage per warp
+static_assert(kDeqWarps == 8 || kDeqWarps == 16, "dequantiser split");
 constexpr int kAcc = 4;          // independent accumulators per tile (K-steps rotate over them)
 constexpr int kTmemCols = 512;   // A stages at columns 0, 128, 256; accumulators from column 384
 constexpr int kDCol = kAbStages * kACols;
@@ -403,12 +406,13 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
         // (K 0..127) for their quarter and warps 10..13 columns 64..127.  The
         // raw codes were stored 128-byte swizzled by the TMA, so the 16-byte
         // loads of 32 consecutive rows are bank-conflict free.
-        const int t = threadIdx.x - 6 * 32;  // 0..255
-        const int quarter = warp & 3, khalf = (warp - 6) >> 2;
+        const int t = threadIdx.x - 6 * 32;  // 0 .. 32 kDeqWarps - 1
+        const int quarter = warp & 3, kpart = (warp - 6) >> 2;
         const int row = quarter * 32 + lane;
-        const int xb = t >> 4, xp = t & 15;  // B row / 16-element part of the hidden slice
+        constexpr int kXPer = kN * kKa / (kDeqWarps * 32);  // hidden-slice elements per thread and stage
+        const int xb = t / (kDeqWarps * 2), xp = t % (kDeqWarps * 2);  // B row / kXPer-element part
         const float up = s_up[xb];
-        const uint32_t tmem_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(khalf * (kACols / 2));
+        const uint32_t tmem_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(kpart * kPartCols);
         uint32_t rit = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < a.n_tiles && ok; tile += gridDim.x) {
@@ -421,13 +425,20 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
                     const int as = abit % kAbStages;
                     if (!mbar_wait(&bars->ab_empty[as], ((abit / kAbStages) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     tc_after();
-                    const int c0 = h * 8 + khalf * 4;  // first 16-byte code chunk (of 16 in the raw row)
-                    uint32_t sc8[2];                   // scales of blocks 2*c0 .. 2*c0+7
-                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                                 : "=r"(sc8[0]), "=r"(sc8[1])
-                                 : "r"(raw + (uint32_t)(kRawCodes + row * (kKs / 16) + 2 * c0)));
+                    constexpr int kChunks = kPartCols / 16;     // 16-byte code chunks (32 weights) per warp
+                    const int c0 = h * 8 + kpart * kChunks;   // first chunk (of 16 in the raw row)
+                    uint32_t sc8[kChunks / 2];                // scales of blocks 2*c0 .. 2*c0 + 2*kChunks - 1
+                    if constexpr (kChunks == 4) {
+                        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                                     : "=r"(sc8[0]), "=r"(sc8[kChunks / 2 - 1])
+                                     : "r"(raw + (uint32_t)(kRawCodes + row * (kKs / 16) + 2 * c0)));
+                    } else {
+                        asm volatile("ld.shared.u32 %0, [%1];"
+                                     : "=r"(sc8[0])
+                                     : "r"(raw + (uint32_t)(kRawCodes + row * (kKs / 16) + 2 * c0)));
+                    }
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {  // 64 weights -> 32 TMEM columns each
+                    for (int half = 0; half < kChunks / 2; ++half) {  // 64 weights -> 32 TMEM columns each
                         const uint32_t sc4 = sc8[half];
                         const uint32_t s01 = e4m3x2_h2(sc4 & 0xFFFFu), s23 = e4m3x2_h2(sc4 >> 16);
                         uint32_t out[32];
@@ -455,14 +466,14 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
                         tmem_st32(tmem_row + (uint32_t)(as * kACols + half * 32), out);
                     }
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {  // hidden slice [16][256] bf16 -> f16 B tile (rows >= nb are zeros)
-                        const int kx = h * kKa + xp * 16 + e * 8;  // element within the raw stage
+                    for (int e = 0; e < kXPer / 8; ++e) {  // hidden slice [16][256] bf16 -> f16 B tile (rows >= nb: zeros)
+                        const int kx = h * kKa + xp * kXPer + e * 8;  // element within the raw stage
                         const uint32_t src = raw + (uint32_t)(kRawCodes + kRawScales + (kx / kXBox) * (kN * kXBox * 2) +
                                                               xb * (kXBox * 2) + (kx % kXBox) * 2);
                         uint32_t pr[4];
                         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                                      : "=r"(pr[0]), "=r"(pr[1]), "=r"(pr[2]), "=r"(pr[3]) : "r"(src));
-                        const int piece = 2 * xp + e;  // 8-element piece of the stage (4 atoms of 8)
+                        const int piece = xp * (kXPer / 8) + e;  // 8-element piece of the stage (4 atoms of 8)
                         const uint32_t b_addr = smem_u32(b_ring + (size_t)as * kBBytes) + (uint32_t)(piece >> 3) * kAtomB +
                                                 (uint32_t)xb * 128u + (uint32_t)(((piece & 7) ^ (xb & 7)) * 16);
                         sts128(b_addr, f32x2_h2(bf_lo(pr[0]) * up, bf_hi(pr[0]) * up),
