@@ -267,7 +267,8 @@ def test_nvfp4_hand_worked_rows(vh):
 
 
 @pytest.mark.parametrize("Vc,H,B", [(1, 64, 1), (777, 128, 1), (4097, 256, 2), (3000, 4096, 8), (1500, 1024, 11),
-                                    (1, 256, 1), (5003, 256, 1), (3001, 1024, 1), (999, 8192, 1), (40_000, 4096, 1)])
+                                    (1, 256, 1), (5003, 256, 1), (3001, 1024, 1), (999, 8192, 1), (40_000, 4096, 1),
+                                    (2000, 512, 16), (1000, 512, 17), (300, 1536, 2)])
 def test_nvfp4_shapes(vh, orc, syn, Vc, H, B):
     cand = syn.sorted_subset(Vc, 2, 248_320, Vc)
     w = syn.normal_f32(Vc, 6, (Vc, H), 0.02)
@@ -335,8 +336,10 @@ def test_verify_tiny_workload(vh, orc, syn, path):
 
 
 @pytest.mark.parametrize("path", [0, 1, 2])
+# rows 8 / 9 switch AUTO from CUDA cores to tensor cores; 128 / 129 from one CTA to the CTA pair
 @pytest.mark.parametrize("B,k,V,H", [(1, 1, 1000, 64), (5, 3, 1000, 128), (3, 2, 129, 192), (64, 3, 3000, 256),
-                                     (40, 3, 2049, 512), (20, 5, 700, 128), (1, 15, 517, 64)])
+                                     (40, 3, 2049, 512), (20, 5, 700, 128), (1, 15, 517, 64), (2, 3, 1000, 128),
+                                     (32, 3, 1300, 192), (43, 2, 900, 128)])
 def test_verify_shapes(vh, orc, syn, path, B, k, V, H):
     W = syn.normal_bf16(V + H, 1, (V, H), 0.02)
     X = syn.normal_bf16(B + k, 4, (B * (k + 1), H), 1.0)
@@ -528,7 +531,7 @@ def check_verify_nvfp4(vh, orc, syn, X, q, s, g, B, k, seed):
 @pytest.mark.parametrize("B,k,V,H", [(1, 3, 1000, 512), (4, 3, 3000, 1024), (5, 3, 2000, 512), (3, 2, 700, 256),
                                      (2, 1, 129, 64), (16, 3, 1500, 512), (33, 3, 2500, 512), (64, 3, 1100, 1024),
                                      (75, 3, 900, 512), (16, 3, 3000, 2048), (20, 3, 40_000, 512),
-                                     (7, 15, 1300, 512)])
+                                     (7, 15, 1300, 512), (9, 1, 800, 512), (32, 3, 1300, 512), (43, 2, 900, 1024)])
 def test_verify_nvfp4_shapes(vh, orc, syn, B, k, V, H):
     w = syn.normal_f32(V + H, 6, (V, H), 0.02)
     q, s, g = syn.nvfp4_quantize(w)
