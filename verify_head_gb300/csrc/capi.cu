@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/verifyhead.h"
 #include "vh_kernels.h"
@@ -27,19 +28,19 @@ inline int gemv_group(int H) {
 }
 
 vh_status check_device() {
-    static int ok_cache[64] = {};  // 1: device already checked
+    static std::atomic<int> ok_cache[64] = {};  // 1: device already checked
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         cudaGetLastError();
         return VH_ERR_DEVICE;
     }
-    if (dev < 64 && ok_cache[dev]) return VH_OK;
+    if (dev < 64 && ok_cache[dev].load(std::memory_order_relaxed)) return VH_OK;
     int major = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess || major < 10) {
         cudaGetLastError();
         return VH_ERR_DEVICE;
     }
-    if (dev < 64) ok_cache[dev] = 1;
+    if (dev < 64) ok_cache[dev].store(1, std::memory_order_relaxed);
     return VH_OK;
 }
 

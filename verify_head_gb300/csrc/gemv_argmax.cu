@@ -19,6 +19,10 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "vh_kernels.h"
 #include "vh_ptx.cuh"
@@ -646,13 +650,39 @@ __global__ void __launch_bounds__(kThreads) k_gemv_nvfp4(const GemvArgs a) {
 constexpr int kMaxDev = 64;
 
 int sm_count() {
-    static int cache[kMaxDev] = {};
+    static std::atomic<int> cache[kMaxDev] = {};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < kMaxDev && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < kMaxDev) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < kMaxDev) cache[dev] = n;
+    if (dev >= 0 && dev < kMaxDev) cache[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+// Resident CTAs per SM of `kernel` at `smem` bytes of dynamic shared memory on
+// the current device, queried once per (kernel, smem, device).
+static cudaError_t occupancy(const void* kernel, size_t smem, int& per_sm) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, size_t, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const auto key = std::make_tuple(kernel, smem, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto it = cache.find(key);
+        if (it != cache.end()) {
+            per_sm = it->second;
+            return cudaSuccess;
+        }
+    }
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = per_sm;
+    return cudaSuccess;
 }
 
 template <typename K>
@@ -661,22 +691,9 @@ static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    // resident CTAs per SM for this kernel and shared-memory size (cached per device)
-    static int occ_cache[kMaxDev] = {};
-    static size_t occ_smem[kMaxDev] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     int per_sm = 0;
-    if (dev >= 0 && dev < kMaxDev && occ_cache[dev] > 0 && occ_smem[dev] == smem) {
-        per_sm = occ_cache[dev];
-    } else {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDev) {
-            occ_smem[dev] = smem;
-            occ_cache[dev] = per_sm;
-        }
-    }
+    cudaError_t oe = occupancy(reinterpret_cast<const void*>(kernel), smem, per_sm);
+    if (oe != cudaSuccess) return oe;
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
     // one resident wave; each warp gets a contiguous, equal share of rows

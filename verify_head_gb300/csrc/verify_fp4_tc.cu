@@ -47,6 +47,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "vh_kernels.h"
@@ -699,17 +700,16 @@ static cudaError_t launch_pair(const CUtensorMap& map_q, const CUtensorMap& map_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(sm_count() / 2, a.n_ptiles)));
-    static int clusters_cache[2][64] = {};  // per kernel instantiation and device
+    static std::atomic<int> clusters_cache[64] = {};  // per device (one per instantiation of this template)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    int& clusters = clusters_cache[N == 256][dev & 63];
+    int clusters = clusters_cache[dev & 63].load(std::memory_order_relaxed);
     if (clusters < 1) {
-        int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, k_verify_fp4_pair<N>, &cfg) != cudaSuccess || c < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, k_verify_fp4_pair<N>, &cfg) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             return cudaErrorNotSupported;
         }
-        clusters = c;
+        clusters_cache[dev & 63].store(clusters, std::memory_order_relaxed);
     }
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(clusters, a.n_ptiles)));
     cfg.numAttrs = 2;

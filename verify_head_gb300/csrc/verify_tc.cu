@@ -31,6 +31,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "vh_kernels.h"
@@ -680,10 +681,16 @@ static cudaError_t launch_verify_tc2(const uint16_t* X, int R, int H, const uint
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(sm_count() / 2, a.n_tiles)));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, k_verify_tc2, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        return cudaErrorNotSupported;
+    static std::atomic<int> clusters_cache[64] = {};  // resident pairs, per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int clusters = clusters_cache[dev & 63].load(std::memory_order_relaxed);
+    if (clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, k_verify_tc2, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            return cudaErrorNotSupported;
+        }
+        clusters_cache[dev & 63].store(clusters, std::memory_order_relaxed);
     }
     cfg.gridDim = dim3(2u * (unsigned)std::max(1, std::min(clusters, a.n_tiles)));
     return cudaLaunchKernelEx(&cfg, k_verify_tc2, map_w, map_x, a);
