@@ -31,6 +31,35 @@ def test_shard_rows_cover():
         assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
 
 
+@pytest.mark.parametrize("world", [2, 3, 4, 5, 8])
+def test_merge_of_shard_argmaxes_equals_global(world):
+    """The oracle's head split into `world` contiguous shards: merging the
+    per-shard (max, global id) pairs gives the single-table argmax, including
+    an exact tie planted across every shard boundary."""
+    import oracle
+    import synth
+    oracle.build()
+    synth.build()
+    draft, _, _ = synth.tiny_case()
+    W, cand = draft.W.copy(), draft.cand_ids
+    x = draft.hidden[0]
+    xf = (x[0].astype(np.uint32) << 16).view(np.float32)
+    win = np.where(xf > 0, 0x3F00, 0xBF00).astype(np.uint16)
+    for r in range(1, world):  # same winning row at the first row of every shard but the first
+        W[shard_rows(cand.size, r, world)[0]] = win
+    W[shard_rows(cand.size, 1, world)[0] - 1] = win  # and at the last row of shard 0
+    ml_r, ids_r = [], []
+    for r in range(world):
+        lo, hi = shard_rows(cand.size, r, world)
+        ids, ml, _ = oracle.draft_argmax(x, W[lo:hi], cand[lo:hi], nthreads=1)
+        ids_r.append(ids)
+        ml_r.append(ml)
+    win_ids, best = merge_rank_argmax(torch.from_numpy(np.stack(ml_r)), torch.from_numpy(np.stack(ids_r)))
+    want_ids, want_ml, _ = oracle.draft_argmax(x, W, cand, nthreads=1)
+    assert int(win_ids[0]) == int(want_ids[0]) == int(cand[shard_rows(cand.size, 1, world)[0] - 1])
+    assert float(best[0]) == float(want_ml[0])
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
@@ -85,3 +114,35 @@ def test_split_v_on_cpu_ranks(tmp_path, world):
         assert r[0] == r[2] and r[1] == r[3]  # merged == single-table argmax
         assert r[0] == r[4]                   # the tie across ranks went to the lower id
     assert all(np.array_equal(res[0], r) for r in res)
+
+
+def _dead_rank_main(rank, world, port, out_dir):
+    import datetime
+
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        return  # this rank dies before the exchange: no all-gather, no clean shutdown
+    outcome = "returned"
+    try:
+        split_v_draft_argmax(lambda: (torch.zeros(1, dtype=torch.int32), torch.zeros(1)))
+    except Exception as e:  # the surviving rank must see an error, not hang
+        outcome = "raised " + type(e).__name__
+    with open(os.path.join(out_dir, "r0.txt"), "w") as f:
+        f.write(outcome)
+
+
+def test_split_v_dead_rank_raises(tmp_path):
+    """A rank that exits before the exchange: the surviving rank's merge raises
+    (peer closed or process-group timeout) instead of waiting forever."""
+    import time
+    port = _free_port()
+    t0 = time.time()
+    ctx = mp.start_processes(_dead_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=False,
+                             start_method="spawn")
+    while not ctx.join(timeout=60):
+        assert time.time() - t0 < 120, "ranks did not finish"
+    out = open(os.path.join(tmp_path, "r0.txt")).read()
+    assert out.startswith("raised"), out
