@@ -335,7 +335,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = cpu_baseline(case, seconds=args.cpu_seconds)
+        cpu = cpu_baseline(case, seconds=args.cpu_seconds, threads=args.oracle_threads)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -376,6 +376,8 @@ def run_ours(args):
 def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"):
     dev = torch.device("cuda")
     out = {}
+    if only == "tiny":
+        out["tiny"] = measure_tiny(torch, vh, synth, timer)
     if only in ("all", "verify"):
         out.update(measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=(only == "verify")))
     if only in ("all", "sweep"):
@@ -389,6 +391,38 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"
     if only in ("all", "nvfp4"):
         out["nvfp4"] = measure_nvfp4(torch, vh, synth, timer, peaks)
     return out
+
+
+def measure_tiny(torch, vh, synth, timer):
+    """The tiny oracle check (4,096 x 256 head, 1,024 candidates, 3 draft steps,
+    verify of 1 x 4 rows): GPU results against the oracle, and call times."""
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda")
+    draft, verify, W_full = synth.tiny_case()
+
+    def t_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    W, cand = t_bf16(draft.W), torch.from_numpy(draft.cand_ids).to(dev)
+    ids_ok = 0
+    for h in draft.hidden:
+        g_ids, _ = vh.mtp_draft_head_argmax(t_bf16(h), W, cand)
+        o_ids, _, _ = oracle.draft_argmax(h, draft.W, draft.cand_ids)
+        ids_ok += int(int(g_ids.item()) == int(o_ids[0]))
+    _, o_nid, _, _ = oracle.verify_greedy(verify.X, W_full, None, 1, 3)
+    d = verify.draft_ids_from(o_nid)
+    acc, nid, _ = vh.spec_verify_greedy(t_bf16(verify.X), t_bf16(W_full), torch.from_numpy(d).to(dev), 1, 3)
+    o_acc = oracle.accept_len(o_nid[:3], d[0])
+    x0 = t_bf16(draft.hidden[0])
+    us_d = timer.time_calls(lambda: vh.mtp_draft_head_argmax(x0, W, cand), 20)
+    Xv, Wv, dv = t_bf16(verify.X), t_bf16(W_full), torch.from_numpy(d).to(dev)
+    us_v = timer.time_calls(lambda: vh.spec_verify_greedy(Xv, Wv, dv, 1, 3), 20)
+    return {"workload": "4,096 x 256 head, 1,024 candidates, B=1 x 3 draft steps; verify 1 x 4 rows (seed 1)",
+            "draft_ids_equal_oracle": f"{ids_ok}/3",
+            "verify_next_ids_equal_oracle": f"{int((nid.cpu().numpy() == o_nid).sum())}/4",
+            "accept_len": int(acc.item()), "oracle_accept_len": int(o_acc),
+            "draft_call_us": stats(us_d), "verify_call_us": stats(us_v)}
 
 
 def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=True):
@@ -610,20 +644,21 @@ def run_single(args):
     print(json.dumps(out), flush=True)
 
 
-def cpu_baseline(case, seconds: float = 10.0):
+def cpu_baseline(case, seconds: float = 10.0, threads: int | None = None):
     """The oracle, as it stands, on the host cores: whole draft steps of the
     same workload until about `seconds` of CPU time have passed."""
     import oracle
     oracle.build()
+    threads = threads or oracle.threads()
     n = 0
     t0 = time.perf_counter()
     while True:
-        oracle.draft_argmax(case.hidden[n % 3], case.W, case.cand_ids)
+        oracle.draft_argmax(case.hidden[n % 3], case.W, case.cand_ids, nthreads=threads)
         n += 1
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 3), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s"}
 
 
@@ -635,14 +670,15 @@ def run_reference(args):
     import oracle
     import synth
     oracle.build()
+    threads = args.oracle_threads or oracle.threads()
     case = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
     for _ in range(max(1, min(args.warmup, 2))):
-        oracle.draft_argmax(case.hidden[0], case.W, case.cand_ids)
+        oracle.draft_argmax(case.hidden[0], case.W, case.cand_ids, nthreads=threads)
     per_step = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
         for i in range(3):
-            oracle.draft_argmax(case.hidden[i], case.W, case.cand_ids)
+            oracle.draft_argmax(case.hidden[i], case.W, case.cand_ids, nthreads=threads)
         per_step.append(time.perf_counter() - t0)
     total = sum(per_step)
     value = 3 * args.steps / total
@@ -651,7 +687,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": WORKLOAD, "Vc": case.Vc, "H": case.H, "B": case.B},
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} bench steps x 3 whole draft steps"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -668,9 +704,15 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "draft", "verify", "sweep", "nvfp4", "gather", "chain", "verify_nvfp4"],
+                    choices=["all", "tiny", "draft", "verify", "sweep", "nvfp4", "gather", "chain", "verify_nvfp4"],
                     help="all = the bench line; others run one measurement only (for profiling)")
+    ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5],
+                    help="one workload by number: 1 tiny oracle check, 2 draft head 65,536 x 2048, "
+                         "3 head-size sweep, 4 batched verify, 5 4-bit draft head")
+    ap.add_argument("--oracle-threads", type=int, default=None, help="host threads for the CPU oracle")
     args = ap.parse_args()
+    if args.config is not None:
+        args.workload = {1: "tiny", 2: "draft", 3: "sweep", 4: "verify", 5: "nvfp4"}[args.config]
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "ours" and args.workload not in ("all", "draft"):

@@ -163,3 +163,12 @@ def test_binding_refuses_cpu_tensors(vh):
     x = torch.zeros(1, 16, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         vh.mtp_draft_head_argmax(x, torch.zeros(4, 16, dtype=torch.bfloat16), torch.arange(4, dtype=torch.int32))
+
+
+def test_debug_build_exports_the_same_symbols(vh):
+    """The VH_DEBUG build (index guards) compiles and exports the same ABI."""
+    from verify_head_gb300 import buildlib
+    path = buildlib.build(debug=True)
+    lib = ctypes.CDLL(path)
+    for n in declared_symbols():
+        assert hasattr(lib, n), n

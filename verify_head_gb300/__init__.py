@@ -11,6 +11,7 @@ Entry points mirror the C ABI in include/verifyhead.h:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -45,50 +46,80 @@ class VHError(RuntimeError):
 
 
 _lib = None
+_debug_lib = None
+_use_debug = False
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
     from . import buildlib as _b
-    return _b.build(force=force, verbose=verbose)
+    return _b.build(force=force, verbose=verbose, debug=debug)
+
+
+def _load(path: str):
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run verify_head_gb300.build() (nvcc, sm_103a)")
+    L = ctypes.CDLL(path)
+    _declare(L)
+    return L
 
 
 def lib():
-    """The loaded library (raises if it has not been built)."""
+    """The loaded library (raises if it has not been built).  Inside
+    `debug_library()` this is the VH_DEBUG build."""
     global _lib
+    if _use_debug:
+        return _debug_lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: run verify_head_gb300.build() (nvcc, sm_103a)")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        L.vh_version.restype = i32
-        L.vh_version.argtypes = []
-        L.vh_status_string.restype = ctypes.c_char_p
-        L.vh_status_string.argtypes = [i32]
-        L.vh_workspace_bytes.restype = sz
-        L.vh_workspace_bytes.argtypes = [i32]
-        L.mtp_draft_head_argmax.restype = i32
-        L.mtp_draft_head_argmax.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
-        L.mtp_draft_head_argmax_nvfp4.restype = i32
-        L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
-        L.spec_verify_greedy.restype = i32
-        L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
-        L.spec_verify_greedy_nvfp4.restype = i32
-        L.spec_verify_greedy_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz,
-                                               vp]
-        L.vh_workspace_error_offset.restype = sz
-        L.vh_workspace_error_offset.argtypes = []
-        L.vh_selftest_bounded_wait.restype = i32
-        L.vh_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
-        L.mtp_draft_head_argmax_gather.restype = i32
-        L.mtp_draft_head_argmax_gather.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
-        L.mtp_draft_head_argmax_static_ws.restype = i32
-        L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
-        L.vh_verify_nvfp4_workspace_bytes.restype = sz
-        L.vh_verify_nvfp4_workspace_bytes.argtypes = [i32, i32]
-        L.spec_verify_greedy_path.restype = i32
-        L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Route every call in the block through libverifyhead_debug.so (built on
+    first use): the same kernels with device-side index guards that set bit 2
+    of the workspace error word instead of touching memory out of range."""
+    global _debug_lib, _use_debug
+    if _debug_lib is None:
+        from . import buildlib as _b
+        _debug_lib = _load(_b.build(debug=True))
+    prev, _use_debug = _use_debug, True
+    try:
+        yield _debug_lib
+    finally:
+        _use_debug = prev
+
+
+def _declare(L):
+    """ctypes signatures of every exported entry point."""
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.vh_version.restype = i32
+    L.vh_version.argtypes = []
+    L.vh_status_string.restype = ctypes.c_char_p
+    L.vh_status_string.argtypes = [i32]
+    L.vh_workspace_bytes.restype = sz
+    L.vh_workspace_bytes.argtypes = [i32]
+    L.mtp_draft_head_argmax.restype = i32
+    L.mtp_draft_head_argmax.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.mtp_draft_head_argmax_nvfp4.restype = i32
+    L.mtp_draft_head_argmax_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_greedy.restype = i32
+    L.spec_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.spec_verify_greedy_nvfp4.restype = i32
+    L.spec_verify_greedy_nvfp4.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                           vp]
+    L.vh_workspace_error_offset.restype = sz
+    L.vh_workspace_error_offset.argtypes = []
+    L.vh_selftest_bounded_wait.restype = i32
+    L.vh_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
+    L.mtp_draft_head_argmax_gather.restype = i32
+    L.mtp_draft_head_argmax_gather.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.mtp_draft_head_argmax_static_ws.restype = i32
+    L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    L.vh_verify_nvfp4_workspace_bytes.restype = sz
+    L.vh_verify_nvfp4_workspace_bytes.argtypes = [i32, i32]
+    L.spec_verify_greedy_path.restype = i32
+    L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
 
 
 def status_string(status: int) -> str:
@@ -104,8 +135,9 @@ def vh_verify_nvfp4_workspace_bytes(rows: int, H: int) -> int:
 
 
 def workspace_error(ws) -> int:
-    """The error word of a workspace tensor (nonzero: a bounded wait expired in
-    some call that used it).  Copies 4 bytes to the host (synchronising)."""
+    """The error word of a workspace tensor: 0, or bit 1 (a bounded wait
+    expired) and / or bit 2 (an index guard of the debug build fired) set by
+    some call that used it.  Copies 4 bytes to the host (synchronising)."""
     off = int(lib().vh_workspace_error_offset())
     return int(ws[off:off + 4].cpu().view(__import__("torch").int32).item())
 

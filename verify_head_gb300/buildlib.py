@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libverifyhead.so")
+LIB_DEBUG = os.path.join(HERE, "libverifyhead_debug.so")  # -DVH_DEBUG: device-side index guards
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,23 +40,28 @@ def _deps():
         glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libverifyhead.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link libverifyhead.so (debug: libverifyhead_debug.so with
+    -DVH_DEBUG, whose kernels guard their indices and report failures in the
+    workspace error word); returns its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    obj_dir = os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     nv = nvcc()
+    flags = list(extra_flags) + (["-DVH_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [nv, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+        cmd = [nv, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,16 +76,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if log.strip():
                 print(log)
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

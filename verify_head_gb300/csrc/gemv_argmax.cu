@@ -98,6 +98,7 @@ __device__ __forceinline__ void finish_argmax(const unsigned long long (&best)[N
     __threadfence();
     if (threadIdx.x < a.nb) {
         unsigned long long k = atomicExch(a.ws.keys + threadIdx.x, 0ull);
+        vh_guard(k != 0ull || a.gather, a.err);  // every row of a candidate table has a winner
         a.ids[threadIdx.x] = (int32_t)key_gid(k);
         if (a.maxlogit != nullptr) a.maxlogit[threadIdx.x] = key_score(k);
     }
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
             (RPI > 1 && r + 1 < r1)
                 ? (a.gather ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r + 1 - r0) & 31)) : r + 1)
                 : 0;
-        const bool ok0 = in_range(pr0);
+        const bool ok0 = in_range(pr0) && vh_guard(a.gather || pr0 < a.n_rows, a.err);
         const bool two = RPI > 1 && (r + 1 < r1) && in_range(pr1);
         const uint16_t* w0p = W + (size_t)(ok0 ? pr0 : 0) * H;
         const uint16_t* w1p = W + (size_t)(two ? pr1 : 0) * H;
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, (CPL >= 4 ? 1 : 2)) k_gemv_nvfp4_dir
     }
 
     unsigned long long best = 0ull;
-    for (long long r = r0; r < r1; r += 2) {
+    for (long long r = r0; r < r1 && vh_guard(r1 <= a.n_rows, a.err); r += 2) {
         const bool two = (r + 1 < r1);
         U32x8 q0[CPL], q1[CPL];
         uint32_t s0[CPL], s1[CPL];
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_gemv_nvfp4_xs(const GemvArgs a)
     const uint32_t xbase = ptx::smem_u32(xsh);
 
     unsigned long long best = 0ull;
-    for (long long r = r0; r < r1; r += 2) {
+    for (long long r = r0; r < r1 && vh_guard(r1 <= a.n_rows, a.err); r += 2) {
         const bool two = (r + 1 < r1);
         U32x8 q0[2], q1[2];
         uint32_t s0[2], s1[2];

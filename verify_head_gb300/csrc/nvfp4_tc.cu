@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
                 best_g = (uint32_t)(row0 + __ffs(bal[0]) - 1);
             }
         }
-        if (lane < a.nb && best_g != 0xFFFFFFFFu) {
+        if (lane < a.nb && best_g != 0xFFFFFFFFu && vh_guard(best_g < (uint32_t)a.Vc, a.err)) {
             const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + best_g) : best_g;
             atomicMax(&merge[lane], make_key(best_v, gid));
         }
@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(kThreadsFp4, 1)
     __threadfence();
     if (threadIdx.x < a.nb) {
         const unsigned long long k = atomicExch(a.ws.keys + threadIdx.x, 0ull);
+        vh_guard(k != 0ull, a.err);  // every hidden row has a winner
         a.ids[threadIdx.x] = (int32_t)key_gid(k);
         if (a.maxlogit != nullptr) a.maxlogit[threadIdx.x] = key_score(k);
     }

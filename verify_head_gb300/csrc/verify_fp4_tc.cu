@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int g = 0; g < kG; ++g) {
             const int col = g * 32 + lane;
-            if (best_g[g] != 0xFFFFFFFFu && col < a.R)
+            if (best_g[g] != 0xFFFFFFFFu && col < a.R && vh_guard(best_g[g] < (uint32_t)a.V, a.err))
                 atomicMax(&merge[col], make_key(best_v[g] * __ldg(a.colscale + col), best_g[g]));
         }
     } else if (warp == 6) {
@@ -605,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
         const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
+        vh_guard(k != 0ull, a.err);  // every hidden row has a winner
         a.next_ids[r] = (int32_t)key_gid(k);
         if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
     }

@@ -346,6 +346,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __threadfence();
     for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
         const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
+        vh_guard(k != 0ull, a.err);  // every hidden row has a winner
         a.next_ids[r] = (int32_t)key_gid(k);
         if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
     }
@@ -579,7 +580,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
 #pragma unroll
         for (int g = 0; g < kMaxN / 32; ++g)
-            if (best_g[g] != 0xFFFFFFFFu) atomicMax(&merge[g * 32 + lane], make_key(best_v[g], best_g[g]));
+            if (best_g[g] != 0xFFFFFFFFu && vh_guard(best_g[g] < (uint32_t)a.V, a.err))
+                atomicMax(&merge[g * 32 + lane], make_key(best_v[g], best_g[g]));
     }
 
     // ---------------- pair teardown, publish, last-CTA decode ----------------
@@ -601,6 +603,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __threadfence();
     for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
         const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
+        vh_guard(k != 0ull, a.err);  // every hidden row has a winner
         a.next_ids[r] = (int32_t)key_gid(k);
         if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
     }

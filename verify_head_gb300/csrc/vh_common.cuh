@@ -62,7 +62,7 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 // Workspace layout: a 16-byte header (uint32 ticket counter at byte 0, uint32
 // error word at byte 4, 8 bytes unused) followed by keys[rows] (uint64).  The
 // caller zeroes it once; every kernel leaves ticket and keys zeroed again.
-// The error word is only ever set (by a wait that gave up), never cleared.
+// The error word is only ever set (bits below), never cleared by a kernel.
 
 struct Workspace {
     unsigned long long* keys;
@@ -74,6 +74,21 @@ constexpr size_t kWsErrorOffset = 4;
 __host__ __device__ constexpr size_t ws_keys_bytes(int rows) { return ((size_t)rows * 8 + 15) / 16 * 16; }
 __host__ __device__ constexpr size_t ws_total_bytes(int rows) { return kWsHeaderBytes + ws_keys_bytes(rows); }
 __host__ __device__ constexpr size_t round16(size_t n) { return (n + 15) / 16 * 16; }
+
+// Error-word bits.  kErrTimeout: a bounded wait gave up.  kErrIndex: a
+// device-side index guard of the VH_DEBUG build failed (the access was
+// skipped).  In the normal build every guard is the constant `true`.
+constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrIndex = 2u;
+
+#ifdef VH_DEBUG
+__device__ __forceinline__ bool vh_guard(bool ok, unsigned int* err) {
+    if (!ok) atomicOr(err, kErrIndex);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool vh_guard(bool, unsigned int*) { return true; }
+#endif
 
 // Views of a workspace base pointer (the row count does not move anything).
 __host__ __device__ inline Workspace ws_view(void* base) {
