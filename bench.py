@@ -26,6 +26,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -75,7 +76,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples (the JSON line carries their summary); VH_BENCH_LOG_DIR overrides the location
+        log_dir = os.environ.get("VH_BENCH_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"vh_clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
