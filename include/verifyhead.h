@@ -28,7 +28,12 @@
  *    consecutive calls in one stream (or a captured CUDA graph) can reuse it
  *    with no memset.  Calls that may overlap in time (different streams)
  *    need different workspaces.
- *  - No global state: calls are thread-safe given distinct workspaces.
+ *  - No global state beyond thread-safe caches of per-device launch facts
+ *    (SM count, occupancy): calls are thread-safe given distinct workspaces.
+ *  - The same sources also build as libverifyhead_debug.so (-DVH_DEBUG): an
+ *    identical ABI whose kernels check their row indices on the device and
+ *    report a failed check in the workspace error word (bit 2) instead of
+ *    touching memory out of range.
  */
 #ifndef VERIFYHEAD_H
 #define VERIFYHEAD_H
@@ -203,13 +208,14 @@ VH_API vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void*
                                                  void* stream);
 
 /*
- * Error word of the workspace.  The tensor-core kernels bound every internal
- * wait (about 2 s); if one expires (e.g. the GPU is oversubscribed or another
- * process holds its tensor memory) the kernel stops early, writes a nonzero
- * 32-bit value at byte offset vh_workspace_error_offset() of `ws` (the same
- * offset for every workspace size), and the outputs of that call are invalid.
- * The library never clears this word: the caller may read it (one 4-byte
- * copy) and reset it.
+ * Error word of the workspace: a 32-bit value at byte offset
+ * vh_workspace_error_offset() of `ws` (the same offset for every workspace
+ * size).  Bit 1: a bounded internal wait of a tensor-core kernel expired
+ * (about 2 s; e.g. the GPU is oversubscribed or another process holds its
+ * tensor memory) and the kernel stopped early.  Bit 2 (debug build only): a
+ * device-side index check failed and the access was skipped.  Either way the
+ * outputs of that call are invalid.  The library never clears this word: the
+ * caller may read it (one 4-byte copy) and reset it.
  */
 VH_API size_t vh_workspace_error_offset(void);
 
