@@ -613,6 +613,8 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
 
 
 def measure_nvfp4(torch, vh, synth, timer, peaks):
+    """4-bit draft head 65,536 x 4096 at B = 1 and B = 8: three draft steps
+    per chain as in the bench step (per call = chain / 3), and single calls."""
     dev = torch.device("cuda")
 
     def t_bf16(bits):
@@ -620,20 +622,29 @@ def measure_nvfp4(torch, vh, synth, timer, peaks):
 
     nv = {}
     for B in (1, 8):
-        c = synth.nvfp4_case(Vc=65_536, H=4096, B=B, steps=1, seed=5)
+        c = synth.nvfp4_case(Vc=65_536, H=4096, B=B, steps=3, seed=5)
         q = torch.from_numpy(c.q).to(dev)
         s = torch.from_numpy(c.s).to(dev)
         cc = torch.from_numpy(c.cand_ids).to(dev)
-        x = t_bf16(c.hidden[0])
+        xs = [t_bf16(h) for h in c.hidden]
         wsb = vh.workspace(B)
-        us = timer.time_calls(lambda: vh.mtp_draft_head_argmax_nvfp4(x, q, s, c.g, cc, ws=wsb), 20)
-        med = statistics.median(us)
-        nbytes = c.q.nbytes + c.s.nbytes + 65_536 * 4 + B * 4096 * 2
-        nv[f"B{B}"] = {"steps_per_s": round(1e6 / med, 1), **stats(us),
-                       "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
-                       "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
-    return nv
+        ids = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(3)]
+        mls = [torch.empty(B, dtype=torch.float32, device=dev) for _ in range(3)]
 
+        def chain():
+            for k in range(3):
+                vh.mtp_draft_head_argmax_nvfp4(xs[k], q, s, c.g, cc, ids=ids[k], maxlogit=mls[k], ws=wsb)
+
+        us = [t / 3 for t in timer.time_calls(chain, 20)]
+        single = timer.time_calls(lambda: vh.mtp_draft_head_argmax_nvfp4(xs[0], q, s, c.g, cc, ws=wsb), 20)
+        mean = statistics.mean(us)
+        nbytes = c.q.nbytes + c.s.nbytes + 65_536 * 4 + B * 4096 * 2
+        nv[f"B{B}"] = {"timing": "3-call chains, per call", "steps_per_s": round(1e6 / mean, 1), **stats(us),
+                       "hbm_gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
+                       "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                       "single_call_us": stats(single),
+                       "kernel": "k_gemv_nvfp4_xs" if B == 1 else "k_nvfp4_tc"}
+    return nv
 
 def run_single(args):
     """One of the extra measurements on its own (a short profiling target)."""

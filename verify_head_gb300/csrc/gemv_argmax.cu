@@ -451,7 +451,9 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t* r) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 
-__global__ void __launch_bounds__(kThreads, 4) k_gemv_nvfp4_xs(const GemvArgs a) {
+// Three CTAs per SM (80 registers): at four the compiler has 64 registers and
+// spills the two rows' code words, which cost ~14% of the kernel's time.
+__global__ void __launch_bounds__(kThreads, 3) k_gemv_nvfp4_xs(const GemvArgs a) {
     extern __shared__ __align__(16) uint32_t xsh[];  // [nch][8 pieces][4 words], swizzled
     __shared__ float s_xmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
