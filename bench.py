@@ -76,6 +76,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.start = 0
         # the raw samples (the JSON line carries their summary); VH_BENCH_LOG_DIR overrides the location
         log_dir = os.environ.get("VH_BENCH_LOG_DIR") or tempfile.gettempdir()
         self.path = os.path.join(log_dir, f"vh_clocks_rank{index}.csv")
@@ -90,6 +91,12 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            # wait (at most 3 s) for the sampler's first line, then count only what follows:
+            # the samples that fall inside the timed region
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
+            self.start = os.path.getsize(self.path)
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -109,7 +116,13 @@ class ClockSampler:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
-            for line in open(self.path):
+            with open(self.path) as f:
+                text = f.read()
+            lines = text[self.start:].splitlines()
+            window = "timed region"
+            if not any(len(x.split(",")) >= 9 for x in lines):  # region shorter than the sampling interval
+                lines, window = text.splitlines(), "around the timed region (region shorter than one sample)"
+            for line in lines:
                 p = [x.strip() for x in line.split(",")]
                 if len(p) < 9:
                     continue
@@ -126,7 +139,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 # ----------------------------------------------------------------------------
@@ -336,9 +349,17 @@ def run_ours(args):
     if rank == 0 and not args.skip_extra and args.workload == "all":
         extra = measure_extra(torch, vh, synth, timer, peaks, load_verify_golden)
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = cpu_baseline(case, seconds=args.cpu_seconds, threads=args.oracle_threads)
+        cpu, first = cpu_baseline(case, seconds=args.cpu_seconds, threads=args.oracle_threads)
+        # the three timed draft steps against the oracle's (ids exact where the top-1 / top-2 gap > 1e-2)
+        g_ids = [int(t.item()) for t in ids]
+        g_ml = [float(t.item()) for t in mls]
+        ok = sum(1 for i, (o_ids, o_ml, o_sec) in enumerate(first)
+                 if (g_ids[i] == int(o_ids[0]) or float(o_ml[0]) - float(o_sec[0]) <= 1e-2)
+                 and abs(g_ml[i] - float(o_ml[0])) <= 2e-2)
+        parity = {"draft_steps_matching_oracle": f"{ok}/3",
+                  "max_abs_maxlogit_err": round(max(abs(g_ml[i] - float(first[i][1][0])) for i in range(3)), 6)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -368,6 +389,7 @@ def run_ours(args):
         "gpu_launches": n_calls,
         "clocks": sampler.summary(),
         "cpu_baseline": cpu,
+        "parity": parity,
     }
     line.update(extra)
     if rank == 0:
@@ -665,15 +687,18 @@ def cpu_baseline(case, seconds: float = 10.0, threads: int | None = None):
     oracle.build()
     threads = threads or oracle.threads()
     n = 0
+    first = []
     t0 = time.perf_counter()
     while True:
-        oracle.draft_argmax(case.hidden[n % 3], case.W, case.cand_ids, nthreads=threads)
+        r = oracle.draft_argmax(case.hidden[n % 3], case.W, case.cand_ids, nthreads=threads)
+        if n < 3:
+            first.append(r)
         n += 1
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
     return {"value": round(n / dt, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s"}
+            "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s"}, first
 
 
 def run_reference(args):
