@@ -135,8 +135,9 @@ __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefe
 // Rows (per warp) whose lines are prefetched into L2 ahead of the row being
 // loaded: more bytes in flight per SM without more registers.
 constexpr int kPrefetchRows = 1;
+constexpr int kGatherPrefetchRows = 1;  // gathering: rows listed next, prefetched from the id cache (2 was slower)
 
-template <int NB, int RPI>
+template <int NB, int RPI, bool GATHER>
 __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const GemvArgs a) {
     extern __shared__ __align__(16) uint16_t xs[];  // [NB][H]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -148,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
     const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
 
     // physical W row of scan position r (the identity unless gathering)
-    auto wrow = [&](long long r) -> long long { return a.gather ? (long long)__ldg(a.cand + r) : r; };
-    auto in_range = [&](long long pr) -> bool { return !a.gather || (pr >= 0 && pr < a.V); };
+    auto wrow = [&](long long r) -> long long { return GATHER ? (long long)__ldg(a.cand + r) : r; };
+    auto in_range = [&](long long pr) -> bool { return !GATHER || (pr >= 0 && pr < a.V); };
 
     pdl_launch_dependents();
     for (long long r = r0; r < min(r1, r0 + RPI); ++r) {
@@ -176,22 +177,35 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
 
     int idx_cache = 0;  // gathering: row ids of the next 32 scan positions, one per lane
     for (long long r = r0; r < r1; r += RPI) {
-        if (a.gather && ((r - r0) & 31) == 0) {
+        if (GATHER && ((r - r0) & 31) == 0) {
             const long long rr = r + lane;
             idx_cache = rr < r1 ? __ldg(a.cand + rr) : -1;
         }
-        if (kPrefetchRows > 0 && !a.gather) {  // keep rows ahead of the loads in flight to L2
+        if constexpr (kPrefetchRows > 0 && !GATHER) {  // keep rows ahead of the loads in flight to L2
             const long long rp = r + kPrefetchRows * RPI;
             for (int rr = 0; rr < RPI; ++rr)
                 if (rp + rr < r1)
                     for (int c = lane * 8; c < nch; c += 256) prefetch_l2(W + (size_t)(rp + rr) * H + c * 16);
+        } else if constexpr (kPrefetchRows > 0) {
+            // gathering: the next positions' row ids come from the warp's id cache (a shuffle, no load);
+            // a position in the next 32-id block is not prefetched
+#pragma unroll
+            for (int rr = 0; rr < kGatherPrefetchRows * RPI; ++rr) {
+                const long long rp = r + RPI + rr;
+                const int slot = (int)((rp - r0) & 31);
+                if (rp < r1 && rp - r0 < (((r - r0) >> 5) + 1) * 32) {
+                    const int pid = __shfl_sync(0xFFFFFFFFu, idx_cache, slot);
+                    if (pid >= 0 && pid < a.V)
+                        for (int c = lane * 8; c < nch; c += 256) prefetch_l2(W + (size_t)pid * H + c * 16);
+                }
+            }
         }
-        const long long pr0 = a.gather ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r - r0) & 31)) : r;
+        const long long pr0 = GATHER ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r - r0) & 31)) : r;
         const long long pr1 =
             (RPI > 1 && r + 1 < r1)
-                ? (a.gather ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r + 1 - r0) & 31)) : r + 1)
+                ? (GATHER ? (long long)__shfl_sync(0xFFFFFFFFu, idx_cache, (int)((r + 1 - r0) & 31)) : r + 1)
                 : 0;
-        const bool ok0 = in_range(pr0) && vh_guard(a.gather || pr0 < a.n_rows, a.err);
+        const bool ok0 = in_range(pr0) && vh_guard(GATHER || pr0 < a.n_rows, a.err);
         const bool two = RPI > 1 && (r + 1 < r1) && in_range(pr1);
         const uint16_t* w0p = W + (size_t)(ok0 ? pr0 : 0) * H;
         const uint16_t* w1p = W + (size_t)(two ? pr1 : 0) * H;
@@ -221,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
                 }
             }
         }
-        const uint32_t g0 = a.gather ? (uint32_t)pr0 : (a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r);
+        const uint32_t g0 = GATHER ? (uint32_t)pr0 : (a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r);
         const uint32_t g1 =
-            two ? (a.gather ? (uint32_t)pr1 : (a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1))) : 0u;
+            two ? (GATHER ? (uint32_t)pr1 : (a.cand ? (uint32_t)__ldg(a.cand + r + 1) : (uint32_t)(r + 1))) : 0u;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const float s0 = warp_sum(p0[b][0] + p0[b][1]);
@@ -729,9 +743,13 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
     a.V = gather_V;
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit; a.tail = tail;
     a.err = ws.ticket + 1;
-    if (nb == 1) return launch_split_v(k_gemv_bf16<1, 1>, (size_t)H * 2, n_rows, a, s, true);
-#define VH_GEMV_CASE(NBV) \
-    if (nb <= NBV) return launch_split_v(k_gemv_bf16<NBV, 2>, (size_t)NBV * H * 2, n_rows, a, s, true);
+    if (nb == 1)
+        return a.gather ? launch_split_v(k_gemv_bf16<1, 1, true>, (size_t)H * 2, n_rows, a, s, true)
+                        : launch_split_v(k_gemv_bf16<1, 1, false>, (size_t)H * 2, n_rows, a, s, true);
+#define VH_GEMV_CASE(NBV)                                                                                    \
+    if (nb <= NBV)                                                                                           \
+        return a.gather ? launch_split_v(k_gemv_bf16<NBV, 2, true>, (size_t)NBV * H * 2, n_rows, a, s, true)     \
+                        : launch_split_v(k_gemv_bf16<NBV, 2, false>, (size_t)NBV * H * 2, n_rows, a, s, true);
     VH_GEMV_CASE(2)
     VH_GEMV_CASE(4)
     VH_GEMV_CASE(8)
