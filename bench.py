@@ -492,6 +492,19 @@ def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core
             out[name]["kernel"] = "k_verify_tc2 (CTA pair, tcgen05 cta_group::2, fused column argmax + acceptance)"
             out[name]["dram_bytes_per_launch"] = profile_traffic("verify_tc.cu", "verify_tc2_256x248320x2048.txt")
             out[name]["algorithmic_bytes_per_launch"] = nbytes
+    # fewer verified rows against the same head: B sequences x 4 positions, AUTO kernel choice
+    rows = {}
+    for B in (1, 4, 16, 32, 48):
+        R = 4 * B
+        Xs, ds = X[:R].contiguous(), draft[:B].contiguous()
+        ws_r = vh.workspace(R)
+        us = timer.time_calls(lambda: vh.spec_verify_greedy(Xs, Wf, ds, B, 3, ws=ws_r), 5, warmup=2)
+        med = statistics.median(us)
+        nbytes_r = vc.W.nbytes + R * 2048 * 2
+        rows[str(R)] = {"rounds_per_s": round(1e6 / med, 1), "median_us": round(med, 2),
+                        "hbm_frac": round(nbytes_r / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                        "kernel": "k_verify_tc (one CTA)" if R <= 128 else "k_verify_tc2 (CTA pair)"}
+    out["verify_rows"] = rows
     del Wf, X
     return out
 

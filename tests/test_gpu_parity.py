@@ -336,7 +336,7 @@ def test_verify_tiny_workload(vh, orc, syn, path):
 
 
 @pytest.mark.parametrize("path", [0, 1, 2])
-# rows 8 / 9 switch AUTO from CUDA cores to tensor cores; 128 / 129 from one CTA to the CTA pair
+# 8 / 9 rows split the CUDA-core groups; 128 / 129 switch from one CTA to the CTA pair
 @pytest.mark.parametrize("B,k,V,H", [(1, 1, 1000, 64), (5, 3, 1000, 128), (3, 2, 129, 192), (64, 3, 3000, 256),
                                      (40, 3, 2049, 512), (20, 5, 700, 128), (1, 15, 517, 64), (2, 3, 1000, 128),
                                      (32, 3, 1300, 192), (43, 2, 900, 128)])

@@ -179,7 +179,10 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     const uint16_t* X = static_cast<const uint16_t*>(hidden);
     const uint16_t* W = static_cast<const uint16_t*>(W_full);
 
-    bool tensor = (path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && R > kGemvRows && H % 64 == 0);
+    // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
+    // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
+    // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.
+    bool tensor = (path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0);
     const int group = tensor ? kTcRows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += group) {
         const int nr = std::min(group, R - r0);
