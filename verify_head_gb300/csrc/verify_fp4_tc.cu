@@ -163,8 +163,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(unsigned long long* bar, uint3
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        const unsigned long long dt = globaltimer() - t0;
+        if (dt > kErrPollNs && *reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+        if (dt > kTimeoutNs) {
             atomicOr(err, 1u);
             return false;
         }

@@ -9,6 +9,10 @@ namespace ptx {
 
 // Every spin on an mbarrier gives up after this long (ns of %globaltimer).
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
+// A waiter reads the error word (set when another warp gave up) only once it
+// has waited this long: a global load on every poll sits between the phase
+// completing and the waiter seeing it, and cost the one-CTA verify 5%.
+constexpr unsigned long long kErrPollNs = 20000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,14 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
 }
 
 // Bounded wait on a barrier phase.  Returns false (and raises *err) if the
-// phase does not complete in time, or at once if *err is already raised.
+// phase does not complete in time, or if *err is raised by someone else while
+// it has waited longer than kErrPollNs.
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, unsigned int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        const unsigned long long dt = globaltimer() - t0;
+        if (dt > kErrPollNs && *reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+        if (dt > kTimeoutNs) {
             atomicOr(err, 1u);
             return false;
         }
