@@ -183,12 +183,24 @@ def stats(us):
             "p90_us": round(us[(len(us) * 9) // 10], 3), "mean_us": round(sum(us) / len(us), 3)}
 
 
+KERNEL_HEADERS = ("vh_common.cuh", "vh_kernels.h", "vh_ptx.cuh")  # included by every kernel file
+
+
+def source_sha(kernel_file: str) -> str:
+    """First 16 hex digits of sha256 over a kernel file followed by the shared
+    headers it compiles with (the key a profile summary was taken on)."""
+    h = hashlib.sha256()
+    for name in (kernel_file,) + KERNEL_HEADERS:
+        h.update(open(os.path.join(ROOT, "verify_head_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel_file: str, summary: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (sha256 of the .cu file); else None."""
+    the current kernel source (source_sha of the .cu file and the shared
+    headers); else None."""
     try:
-        src = open(os.path.join(ROOT, "verify_head_gb300", "csrc", kernel_file), "rb").read()
-        sha = hashlib.sha256(src).hexdigest()[:16]
+        sha = source_sha(kernel_file)
         vals = {}
         for line in open(os.path.join(ROOT, "profiles", summary)):
             if ":" in line and not line.startswith("#"):
@@ -644,6 +656,16 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
         "workload": "4 seqs x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "kernel": "k_nvfp4_tc",
         "rounds_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
         "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    # 4 rows (one MTP3 sequence) vs the same head
+    X4, d1 = X[:4].contiguous(), d[:1].contiguous()
+    ws = vh.verify_nvfp4_workspace(4, 4096)
+    us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4(X4, q, s, c.g, d1, 1, 3, ws=ws), 20)
+    med = statistics.median(us)
+    nbytes = c.q.nbytes + c.s.nbytes + 4 * 4096 * 2
+    out["head_65536x4096_4_rows"] = {
+        "workload": "1 seq x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "kernel": "k_nvfp4_mma",
+        "rounds_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+        "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
     return out
 
 
@@ -678,7 +700,7 @@ def measure_nvfp4(torch, vh, synth, timer, peaks):
                        "hbm_gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
                        "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                        "single_call_us": stats(single),
-                       "kernel": "k_gemv_nvfp4_xs" if B == 1 else "k_nvfp4_tc"}
+                       "kernel": "k_gemv_nvfp4_xs" if B == 1 else "k_nvfp4_mma"}
     return nv
 
 def run_single(args):

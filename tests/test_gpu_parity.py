@@ -277,6 +277,35 @@ def test_nvfp4_shapes(vh, orc, syn, Vc, H, B):
     check_nvfp4(vh, orc, x, q, s, g, cand)
 
 
+# the warp-level-MMA kernel (2..8 hidden rows per launch, H = 256 * 2^i <= 4096):
+# one partial block, a last block with a single valid row, fewer blocks than
+# SMs, every slice count from 1 to 16, groups of 8 rows with a ragged last group
+@pytest.mark.parametrize("Vc,H,B", [(5, 4096, 3), (17, 2048, 2), (100, 1024, 8), (2049, 512, 9), (33, 256, 24),
+                                    (70_001, 4096, 2)])
+def test_nvfp4_mma_shapes(vh, orc, syn, Vc, H, B):
+    cand = syn.sorted_subset(Vc + 1, 2, 248_320, Vc)
+    q, s, g = syn.nvfp4_quantize(syn.normal_f32(Vc + 2, 6, (Vc, H), 0.02))
+    x = syn.normal_bf16(B + 3, 3, (B, H), 1.0)
+    check_nvfp4(vh, orc, x, q, s, g, cand)
+
+
+def test_nvfp4_mma_ties_lowest_id(vh, orc, syn):
+    """Identical top rows in different blocks, row halves and CTAs score
+    exactly alike: every hidden row gets the lowest candidate id among them."""
+    Vc, H, B = 20_000, 1024, 4
+    q, s, g = syn.nvfp4_quantize(syn.normal_f32(11, 6, (Vc, H), 0.02))
+    top = [7000, 39, 19_999, 2048, 47]
+    q[top] = 0x77  # +6 in every element
+    s[top] = 0x7E  # scale 448
+    cand = syn.sorted_subset(12, 2, 248_320, Vc)
+    x = np.full((B, H), 0x3F80, np.uint16)  # +1.0
+    ids, ml = run_nvfp4(vh, x, q, s, g, cand)
+    assert list(ids) == [int(cand[min(top)])] * B
+    o_ids, o_ml, _ = orc.draft_argmax_nvfp4(x, q, s, g, cand)
+    assert list(o_ids) == list(ids)
+    np.testing.assert_allclose(ml, o_ml, rtol=0, atol=TOL_4BIT)
+
+
 @pytest.mark.parametrize("B", [1, 8])
 def test_nvfp4_full_size_65536x4096(vh, orc, syn, B):
     case = syn.nvfp4_case(Vc=65_536, H=4096, B=B, steps=3 if B == 1 else 1, seed=5)
@@ -525,13 +554,15 @@ def check_verify_nvfp4(vh, orc, syn, X, q, s, g, B, k, seed):
     check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
 
 
-# rows <= 16: one k_nvfp4_tc pass; 17..128 rows: CTA pair with N = 128; 129..256:
+# rows <= 16: warp-level MMAs in groups of 8 (H = 256 * 2^i <= 4096) or one
+# k_nvfp4_tc pass (other H % 512 == 0); 17..128 rows: CTA pair with N = 128; 129..256:
 # N = 256; > 256 rows: groups of 256; H = 2048 wraps the raw-code ring along K;
 # V = 40,000 gives every CTA pair several tiles (accumulator double buffering)
 @pytest.mark.parametrize("B,k,V,H", [(1, 3, 1000, 512), (4, 3, 3000, 1024), (5, 3, 2000, 512), (3, 2, 700, 256),
                                      (2, 1, 129, 64), (16, 3, 1500, 512), (33, 3, 2500, 512), (64, 3, 1100, 1024),
                                      (75, 3, 900, 512), (16, 3, 3000, 2048), (20, 3, 40_000, 512),
-                                     (7, 15, 1300, 512), (9, 1, 800, 512), (32, 3, 1300, 512), (43, 2, 900, 1024)])
+                                     (7, 15, 1300, 512), (9, 1, 800, 512), (32, 3, 1300, 512), (43, 2, 900, 1024),
+                                     (2, 3, 17, 2048), (1, 3, 3001, 1536), (3, 3, 1000, 4096)])
 def test_verify_nvfp4_shapes(vh, orc, syn, B, k, V, H):
     w = syn.normal_f32(V + H, 6, (V, H), 0.02)
     q, s, g = syn.nvfp4_quantize(w)

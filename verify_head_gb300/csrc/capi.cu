@@ -14,6 +14,7 @@ namespace {
 constexpr int kGemvRows = 8;   // hidden rows per CUDA-core launch
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
+constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kMaxDraftB = 256;
 constexpr int kMaxH = 65536;
 
@@ -144,16 +145,22 @@ vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const vh::Workspace w = make_ws(ws, B);
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
-    // one hidden row: CUDA-core streaming GEMV; more: tensor cores when H is a
-    // multiple of the 512-element raw stage, else CUDA cores
-    const bool tc = (B > 1 && H % 512 == 0);
-    const int grp = tc ? kTcFp4Rows : gemv_group(H);
+    // one hidden row: CUDA-core streaming GEMV.  2..8 rows: warp-level MMAs
+    // (H = 256 * 2^i <= 4096).  More rows: tcgen05 in groups of 16 when H is a
+    // multiple of the 512-element raw stage (one pass over the head for 16
+    // rows beats two 8-row MMA passes), else MMA groups of 8, else CUDA cores.
+    const bool mma_ok = vh::nvfp4_mma_supported(kMmaFp4Rows, H);
+    const bool tc = B > 1 && H % 512 == 0 && !(B <= kMmaFp4Rows && mma_ok);
+    const bool mma = B > 1 && !tc && mma_ok;
+    const int grp = mma ? kMmaFp4Rows : tc ? kTcFp4Rows : gemv_group(H);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
-        cudaError_t e = tc ? vh::launch_nvfp4_tc(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w,
-                                                 ids + b0, maxlogit + b0, s)
-                           : vh::launch_gemv_nvfp4(x + (size_t)b0 * H, nb, H, Wq, scales, tensor_scale, cand_ids, Vc,
-                                                   w, ids + b0, maxlogit + b0, s);
+        const uint16_t* xb = x + (size_t)b0 * H;
+        cudaError_t e =
+            mma  ? vh::launch_nvfp4_mma(xb, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w, ids + b0, maxlogit + b0, s)
+            : tc ? vh::launch_nvfp4_tc(xb, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w, ids + b0, maxlogit + b0, s)
+                 : vh::launch_gemv_nvfp4(xb, nb, H, Wq, scales, tensor_scale, cand_ids, Vc, w, ids + b0, maxlogit + b0,
+                                         s);
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;
@@ -249,7 +256,11 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
         if (e != cudaErrorNotSupported) return e == cudaSuccess ? VH_OK : launch_status(e);
         cudaGetLastError();
     }
-    const int grp = tc ? kTcFp4Rows : gemv_group(H);
+    // up to 16 rows (or H off the pair kernel's grid): warp-level MMAs for up
+    // to 8 rows (H = 256 * 2^i <= 4096), tcgen05 groups of 16 for more (or
+    // MMA groups of 8 where H % 512 != 0), else CUDA cores
+    const bool mma = vh::nvfp4_mma_supported(kMmaFp4Rows, H) && (R <= kMmaFp4Rows || !tc);
+    const int grp = mma ? kMmaFp4Rows : tc ? kTcFp4Rows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += grp) {
         const int nr = std::min(grp, R - r0);
         vh::AcceptTail tail;
@@ -261,10 +272,12 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
             tail.k = k;
         }
         float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
-        cudaError_t e = tc ? vh::launch_nvfp4_tc(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, nullptr, V, w,
-                                                 next_ids + r0, ml, s, tail)
-                           : vh::launch_gemv_nvfp4(x + (size_t)r0 * H, nr, H, Wq, scales, tensor_scale, nullptr, V, w,
-                                                   next_ids + r0, ml, s, tail);
+        const uint16_t* xr = x + (size_t)r0 * H;
+        cudaError_t e =
+            mma  ? vh::launch_nvfp4_mma(xr, nr, H, Wq, scales, tensor_scale, nullptr, V, w, next_ids + r0, ml, s, tail)
+            : tc ? vh::launch_nvfp4_tc(xr, nr, H, Wq, scales, tensor_scale, nullptr, V, w, next_ids + r0, ml, s, tail)
+                 : vh::launch_gemv_nvfp4(xr, nr, H, Wq, scales, tensor_scale, nullptr, V, w, next_ids + r0, ml, s,
+                                         tail);
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;

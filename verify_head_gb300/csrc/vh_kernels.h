@@ -39,6 +39,15 @@ cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq,
                             const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
                             const AcceptTail& tail = AcceptTail{});
 
+// Block-scaled 4-bit head on warp-level MMAs fed from registers (codes
+// streamed per warp with cp.async, exact f16 dequantisation, fp32
+// accumulation), nb <= 8 hidden rows, H = 256 * 2^i <= 4096.  Returns
+// cudaErrorNotSupported for other shapes.
+bool nvfp4_mma_supported(int nb, int H);
+cudaError_t launch_nvfp4_mma(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
+                             const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
+                             const AcceptTail& tail = AcceptTail{});
+
 // tcgen05 skinny GEMM + per-row argmax + acceptance scan for R <= 256 hidden
 // rows (H % 64 == 0).  Returns cudaErrorNotSupported when the shape does not
 // fit the kernel.
