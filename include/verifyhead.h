@@ -240,12 +240,13 @@ VH_API size_t vh_verify_nvfp4_workspace_bytes(int rows, int H);
  * entries).  Rows, next_ids, row_maxlogit and accept_len are defined as for
  * spec_verify_greedy, with W_full replaced by the decoded 4-bit head.
  *
- * Kernels (H % 512 == 0): up to 16 rows in one tensor-core pass with N = 16;
- * more rows on a CTA pair (tcgen05 cta_group::2) with N = 128 or 256, up to
- * 256 rows per pass over the head, after converting the hidden rows to f16
- * with a per-row power-of-two prescale into the workspace scratch (exact for
- * every element within 2^31 of its row's largest magnitude).  Other H: CUDA
- * cores, groups of 8 rows.
+ * Kernels: up to 8 rows in one pass of warp-level MMAs fed from registers
+ * (H = 256 * 2^i <= 4096); up to 16 rows in one tcgen05 pass with N = 16
+ * (H % 512 == 0); more rows (H % 512 == 0) on a CTA pair (tcgen05
+ * cta_group::2) with N = 128 or 256, up to 256 rows per pass over the head,
+ * after converting the hidden rows to f16 with a per-row power-of-two
+ * prescale into the workspace scratch (exact for every element within 2^31
+ * of its row's largest magnitude).  Other H: CUDA cores, groups of 8 rows.
  *
  *  hidden        device, bf16 [B*(k+1)][H], 16-byte aligned
  *  Wq, scales    device, uint8 [V][H/2] (32-byte aligned), uint8 [V][H/16] (16-byte aligned)
