@@ -1,7 +1,8 @@
 """Seeded random shapes through every entry point against the oracle: batch
 sizes, widths (every allowed multiple), table sizes, k and gathered id lists
 drawn at random, so that kernel selection boundaries, ragged tails and group
-splits are hit in combinations no hand-picked list covers."""
+splits are hit in combinations no hand-picked list covers (46 cases by
+default; VH_FUZZ_SCALE multiplies every family)."""
 import os
 
 import numpy as np
@@ -143,3 +144,38 @@ def test_fuzz_verify_nvfp4(vh, orc, syn, case):
 
     check_ids(nid, ml.cpu().numpy(), o_nid, o_ml, o_sec, score_of, TOL_4BIT)
     np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid, draft, B, k))
+
+
+@pytest.mark.parametrize("case", range(6 * SCALE))
+def test_fuzz_nvfp4_mma(vh, orc, syn, case):
+    """2..8 rows at every width of the warp-level-MMA kernel (H = 256 * 2^i <=
+    4096), ragged heads: the draft entry point, and verify with at most 8 rows."""
+    import torch
+    rng = np.random.default_rng(1400 + case)
+    H = 256 << int(rng.integers(0, 5))
+    B = int(rng.integers(2, 9))
+    Vc = _rows_for(rng, MAC_BUDGET // 2, B * H, lo=1, hi=30_000)
+    q, s, g = syn.nvfp4_quantize(syn.normal_f32(9700 + case, 6, (Vc, H), 0.02))
+    cand = syn.sorted_subset(9700 + case, 2, 248_320, Vc)
+    x = syn.normal_bf16(9800 + case, 3, (B, H), 1.0)
+    ids, ml = vh.mtp_draft_head_argmax_nvfp4(to_torch_bf16(x), to_torch(q), to_torch(s), g, to_torch(cand))
+    torch.cuda.synchronize()
+    o_ids, o_ml, o_sec = orc.draft_argmax_nvfp4(x, q, s, g, cand)
+
+    def score_of(r, gid):
+        c = int(np.searchsorted(cand, gid))
+        return float(orc.scores_nvfp4(x[r], q[c:c + 1], s[c:c + 1], g, nthreads=1)[0])
+
+    check_ids(ids.cpu().numpy(), ml.cpu().numpy(), o_ids, o_ml, o_sec, score_of, TOL_4BIT)
+
+    k = int(rng.integers(1, 8))
+    Bv = max(1, 8 // (k + 1))
+    X = syn.normal_bf16(9900 + case, 4, (Bv * (k + 1), H), 1.0)
+    draft = rng.integers(0, Vc, size=(Bv, k)).astype(np.int32)
+    acc, nid, vml = vh.spec_verify_greedy_nvfp4(to_torch_bf16(X), to_torch(q), to_torch(s), g, to_torch(draft), Bv, k)
+    torch.cuda.synchronize()
+    _, v_nid, v_ml, v_sec = orc.verify_greedy_nvfp4(X, q, s, g, None, Bv, k)
+    nid = nid.cpu().numpy()
+    check_ids(nid, vml.cpu().numpy(), v_nid, v_ml, v_sec,
+              lambda r, v: float(orc.scores_nvfp4(X[r], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0]), TOL_4BIT)
+    np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid, draft, Bv, k))
