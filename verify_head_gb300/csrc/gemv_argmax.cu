@@ -144,9 +144,11 @@ __global__ void __launch_bounds__(kThreads, (NB == 1 ? 4 : 1)) k_gemv_bf16(const
     const int H = a.H, nch = H >> 4;  // 32-byte chunks per row
     const uint16_t* __restrict__ W = static_cast<const uint16_t*>(a.W);
 
-    const long long gw = (long long)blockIdx.x * kWarps + warp;
-    const long long r0 = gw * a.rows_per_warp;
-    const long long r1 = min(r0 + (long long)a.rows_per_warp, (long long)a.n_rows);
+    // even split of the rows over every warp of the resident wave (13 or 14
+    // rows each for 65,536 rows): every SM streams the same share
+    const long long gw = (long long)blockIdx.x * kWarps + warp, nw = (long long)gridDim.x * kWarps;
+    const long long r0 = gw * a.n_rows / nw;
+    const long long r1 = (gw + 1) * a.n_rows / nw;
 
     // physical W row of scan position r (the identity unless gathering)
     auto wrow = [&](long long r) -> long long { return GATHER ? (long long)__ldg(a.cand + r) : r; };
@@ -703,7 +705,8 @@ static cudaError_t occupancy(const void* kernel, size_t smem, int& per_sm) {
 }
 
 template <typename K>
-static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a, cudaStream_t s, bool pdl) {
+static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a, cudaStream_t s, bool pdl,
+                                  bool even_rows = false) {
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -713,14 +716,18 @@ static cudaError_t launch_split_v(K kernel, size_t smem, int n_rows, GemvArgs& a
     if (oe != cudaSuccess) return oe;
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
-    // one resident wave; each warp gets a contiguous, equal share of rows
+    // one resident wave; each warp gets a contiguous share of rows: with
+    // even_rows the kernel splits n_rows over all grid * kWarps warps (shares
+    // differ by at most one row), else every warp takes rows_per_warp rows
+    // and the grid shrinks to the warps needed
     long long grid = (long long)sms * per_sm;
     const long long min_rows_per_warp = 2;
     const long long max_grid = ((long long)n_rows + kWarps * min_rows_per_warp - 1) / (kWarps * min_rows_per_warp);
     grid = std::max(1LL, std::min(grid, max_grid));
     const long long warps = grid * kWarps;
     a.rows_per_warp = (int)(((long long)n_rows + warps - 1) / warps);
-    grid = ((long long)n_rows + (long long)a.rows_per_warp * kWarps - 1) / ((long long)a.rows_per_warp * kWarps);
+    if (!even_rows)
+        grid = ((long long)n_rows + (long long)a.rows_per_warp * kWarps - 1) / ((long long)a.rows_per_warp * kWarps);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -744,12 +751,12 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
     a.nb = nb; a.H = H; a.n_rows = n_rows; a.ws = ws; a.ids = ids; a.maxlogit = maxlogit; a.tail = tail;
     a.err = ws.ticket + 1;
     if (nb == 1)
-        return a.gather ? launch_split_v(k_gemv_bf16<1, 1, true>, (size_t)H * 2, n_rows, a, s, true)
-                        : launch_split_v(k_gemv_bf16<1, 1, false>, (size_t)H * 2, n_rows, a, s, true);
-#define VH_GEMV_CASE(NBV)                                                                                    \
-    if (nb <= NBV)                                                                                           \
-        return a.gather ? launch_split_v(k_gemv_bf16<NBV, 2, true>, (size_t)NBV * H * 2, n_rows, a, s, true)     \
-                        : launch_split_v(k_gemv_bf16<NBV, 2, false>, (size_t)NBV * H * 2, n_rows, a, s, true);
+        return a.gather ? launch_split_v(k_gemv_bf16<1, 1, true>, (size_t)H * 2, n_rows, a, s, true, true)
+                        : launch_split_v(k_gemv_bf16<1, 1, false>, (size_t)H * 2, n_rows, a, s, true, true);
+#define VH_GEMV_CASE(NBV)                                                                                          \
+    if (nb <= NBV)                                                                                                 \
+        return a.gather ? launch_split_v(k_gemv_bf16<NBV, 2, true>, (size_t)NBV * H * 2, n_rows, a, s, true, true) \
+                        : launch_split_v(k_gemv_bf16<NBV, 2, false>, (size_t)NBV * H * 2, n_rows, a, s, true, true);
     VH_GEMV_CASE(2)
     VH_GEMV_CASE(4)
     VH_GEMV_CASE(8)
