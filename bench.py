@@ -746,8 +746,18 @@ def cpu_baseline(case, seconds: float = 10.0, threads: int | None = None):
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, over a shorter sample
+    n1, t1 = 0, time.perf_counter()
+    while True:
+        oracle.draft_argmax(case.hidden[n1 % 3], case.W, case.cand_ids, nthreads=1)
+        n1 += 1
+        if time.perf_counter() - t1 > min(3.0, seconds / 3):
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(n / dt, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s"}, first
+            "sample": f"{n} whole draft steps (65,536 x 2048 bf16 head, B=1) in {dt:.1f} s",
+            "single_thread": {"value": round(n1 / dt1, 3), "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} whole draft steps in {dt1:.1f} s"}}, first
 
 
 def run_reference(args):
