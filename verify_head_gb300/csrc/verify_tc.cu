@@ -43,16 +43,15 @@ namespace tc {
 constexpr int kBlockM = 128;      // W rows per tile (MMA M)
 constexpr int kBlockK = 64;       // K per stage (one 128 B swizzle atom of bf16)
 constexpr int kMaxN = 256;        // hidden rows per launch (MMA N <= 256)
-constexpr int kStages = 4;
+constexpr int kMaxStagesTc = 6;    // deepest ring of any instance
 constexpr int kThreadsTc = 192;
 constexpr int kEpiWarp0 = 2;
 constexpr int kStageA = kBlockM * kBlockK * 2;  // 16 KiB
-constexpr int kStageB = kMaxN * kBlockK * 2;    // 32 KiB
 constexpr int kTmemCols = 512;                  // two 256-column accumulators
 
 struct alignas(8) Barriers {
-    unsigned long long full[kStages];
-    unsigned long long empty[kStages];
+    unsigned long long full[kMaxStagesTc];
+    unsigned long long empty[kMaxStagesTc];
     unsigned long long tmem_full[2];
     unsigned long long tmem_empty[2];
     unsigned long long mma_done;
@@ -60,8 +59,12 @@ struct alignas(8) Barriers {
     unsigned int pad;
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * (kStageA + kStageB) + sizeof(Barriers) +
-                              kMaxN * 8 /*merge*/ + 64;
+// Shared memory of k_verify_tc<STAGES, NMAX>: a ring of STAGES x (16 KiB of W +
+// NMAX x 128 B of hidden rows).
+__host__ __device__ constexpr size_t smem_bytes_tc(int stages, int nmax) {
+    return 1024 /*alignment slack*/ + (size_t)stages * (kStageA + (size_t)nmax * kBlockK * 2) + sizeof(Barriers) +
+           kMaxN * 8 /*merge*/ + 64;
+}
 
 struct TcArgs {
     int R;        // hidden rows in this launch (1..256)
@@ -190,12 +193,15 @@ __device__ __forceinline__ void column_argmax32(const float (&v)[32], bool valid
 
 // ---------------------------------------------------------------------------
 
+template <int kStages, int NMAX>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_verify_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x, const TcArgs a) {
+    static_assert(kStages <= kMaxStagesTc && NMAX % 8 == 0 && NMAX <= kMaxN, "ring shape");
+    constexpr int kStageB = NMAX * kBlockK * 2;  // hidden rows of one stage (1024-byte multiple)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_a = smem;                                  // kStages x 16 KiB (W tiles)
-    uint8_t* stage_b = smem + (size_t)kStages * kStageA;      // kStages x 32 KiB (hidden rows)
+    uint8_t* stage_b = smem + (size_t)kStages * kStageA;      // kStages x NMAX x 128 B (hidden rows)
     Barriers* bars = reinterpret_cast<Barriers*>(stage_b + (size_t)kStages * kStageB);
     unsigned long long* merge = reinterpret_cast<unsigned long long*>(bars + 1);  // [kMaxN]
     __shared__ unsigned int s_last;
@@ -711,8 +717,6 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     const int N = (R + 15) / 16 * 16;
     alignas(64) CUtensorMap map_w, map_x;
     if (!make_map(&map_w, W, V, H, kBlockM) || !make_map(&map_x, X, R, H, N)) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(k_verify_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
     TcArgs a{};
     a.R = R;
     a.N = N;
@@ -725,8 +729,19 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     a.maxlogit = maxlogit;
     a.tail = tail;
     const int grid = std::max(1, std::min(sm_count(), a.n_tiles));
-    k_verify_tc<<<grid, kThreadsTc, kSmemBytes, s>>>(map_w, map_x, a);
-    return cudaGetLastError();
+    // ring depth by width: 65-128 hidden rows fit six stages (128 rows: 166.9 against
+    // 172-174 us with four); deeper rings for fewer rows measured no better (8 stages at
+    // 64 rows: 170.0 us, as with four) or worse (10 stages at 4-16 rows: 174-176 against
+    // 168-174 us), so up to 64 rows keep four
+    auto go = [&](auto kernel, size_t smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kernel<<<grid, kThreadsTc, smem, s>>>(map_w, map_x, a);
+        return cudaGetLastError();
+    };
+    if (N <= 64) return go(k_verify_tc<4, 64>, smem_bytes_tc(4, 64));
+    if (N <= 128) return go(k_verify_tc<6, 128>, smem_bytes_tc(6, 128));
+    return go(k_verify_tc<4, 256>, smem_bytes_tc(4, 256));
 }
 
 }  // namespace vh
