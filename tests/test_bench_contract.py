@@ -33,3 +33,21 @@ def test_command_line_offers_configs_and_oracle_threads():
     assert r.returncode == 0
     for flag in ("--gpus", "--steps", "--warmup", "--impl", "--config", "--workload", "--oracle-threads"):
         assert flag in r.stdout, flag
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches N > 1 (torchrun, 127.0.0.1): rank 0
+    alone times the oracle and prints the line; the other rank exits 0."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1", "--oracle-threads", "2"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
