@@ -133,10 +133,11 @@ VH_API vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_
  * applied after accumulation (the result equals the per-weight rule up to
  * fp32 rounding).
  *
- * Kernels: one hidden row on CUDA cores; 2..8 rows in one pass of
- * warp-level MMAs fed from registers (H = 256 * 2^i <= 4096); more rows (or
- * other H % 512 == 0) on tcgen05 in passes of 16 rows; other H on CUDA cores
- * in passes of 8 rows.  Every pass reads the whole table once.
+ * Kernels: one hidden row on CUDA cores; 2..8 rows with H = 256 * 2^i <=
+ * 4096 in one pass of warp-level MMAs fed from registers; otherwise tcgen05
+ * passes of 16 rows when H % 512 == 0, warp-level MMA passes of 8 rows when
+ * H == 256, else CUDA-core passes of 8 rows.  Every pass reads the whole
+ * table once.
  *
  *  hidden        device, bf16 [B][H], 16-byte aligned
  *  Wq            device, uint8 [Vc][H/2], 32-byte aligned
