@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -186,12 +187,19 @@ def stats(us):
 KERNEL_HEADERS = ("vh_common.cuh", "vh_kernels.h", "vh_ptx.cuh")  # included by every kernel file
 
 
+_COMMENTS = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def source_sha(kernel_file: str) -> str:
-    """First 16 hex digits of sha256 over a kernel file followed by the shared
-    headers it compiles with (the key a profile summary was taken on)."""
+    """First 16 hex digits of sha256 over the code of a kernel file followed by
+    the shared headers it compiles with (the key a profile summary was taken
+    on).  Comments, trailing blanks and empty lines are left out, so editing a
+    comment does not orphan a profile; any change to the code does."""
     h = hashlib.sha256()
     for name in (kernel_file,) + KERNEL_HEADERS:
-        h.update(open(os.path.join(ROOT, "verify_head_gb300", "csrc", name), "rb").read())
+        text = open(os.path.join(ROOT, "verify_head_gb300", "csrc", name), encoding="utf-8").read()
+        code = "\n".join(ln.rstrip() for ln in _COMMENTS.sub("", text).splitlines() if ln.strip())
+        h.update(code.encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -33,7 +33,7 @@ cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* W
                               cudaStream_t s, const AcceptTail& tail = AcceptTail{});
 
 // Block-scaled 4-bit head on the tensor cores (exact f16 dequantisation,
-// tcgen05 kind::f16), nb <= 16 hidden rows, H % 256 == 0.  Returns
+// tcgen05 kind::f16), nb <= 16 hidden rows, H % 512 == 0.  Returns
 // cudaErrorNotSupported for other shapes.
 cudaError_t launch_nvfp4_tc(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
                             const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
