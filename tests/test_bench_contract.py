@@ -51,3 +51,23 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_profile_key_ignores_comments_only(tmp_path, monkeypatch):
+    """A profile stays keyed to its kernel through comment and blank-line edits;
+    a code edit changes the key."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "verify_head_gb300", "csrc")
+    csrc = tmp_path / "verify_head_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("gemv_argmax.cu",) + bench.KERNEL_HEADERS:
+        (csrc / name).write_text(open(os.path.join(src, name), encoding="utf-8").read(), encoding="utf-8")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.source_sha("gemv_argmax.cu")
+    k = csrc / "gemv_argmax.cu"
+    text = k.read_text(encoding="utf-8")
+    k.write_text("// a new comment\n\n" + text.replace("\n", "  \n", 3) + "\n/* block\n comment */\n", encoding="utf-8")
+    assert bench.source_sha("gemv_argmax.cu") == base
+    k.write_text(text + "\nstatic int vh_unused_for_test = 1;\n", encoding="utf-8")
+    assert bench.source_sha("gemv_argmax.cu") != base
