@@ -630,3 +630,52 @@ def test_verify_nvfp4_accept_cases(vh):
     acc, nid, _ = run_verify_nvfp4(vh, X, q, s, 1.0, draft, B, k)
     assert list(acc) == [c[2] for c in cases]
     assert list(nid) == [t for c in cases for t in c[0]]
+
+
+def _load_golden(name):
+    rows, seqs, meta = {}, {}, {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            p = line.split()
+            if not p or p[0].startswith("#"):
+                continue
+            if p[0] == "row":
+                rows[int(p[1])] = (int(p[2]), float.fromhex(p[3]), float.fromhex(p[4]))
+            elif p[0] == "seq":
+                seqs[int(p[1])] = ([int(v) for v in p[2:-1]], int(p[-1]))
+            else:
+                meta[p[0]] = p[1:]
+    return rows, seqs, meta
+
+
+def test_verify_nvfp4_full_size_all_rows_golden(vh, orc, syn):
+    """64 x 4 rows against the full 248,320 x 2048 4-bit head: all 256 rows
+    and all 64 accept lengths against the stored oracle results
+    (tests/golden/make_verify_nvfp4_golden.py), plus the live oracle on a few
+    sampled rows."""
+    rows, seqs, meta = _load_golden("verify_nvfp4_b64_k3_248320x2048.txt")
+    B, k, V = 64, 3, syn.V_FULL
+    q, s, g = syn.nvfp4_head(seed=2, V=V, H=2048)
+    X = syn.verify_case(B=B, k=k, H=2048, V=V, seed=4, with_head=False).X
+    assert float.fromhex(meta["tensor_scale"][0]) == float(g)
+    assert syn.fingerprint(X) == int(meta["fingerprint_x"][0])
+    sample = [int(v) for v in meta["fingerprint_q_rows"][:-1]]
+    assert syn.fingerprint(np.ascontiguousarray(q[sample])) == int(meta["fingerprint_q_rows"][-1])
+    assert syn.fingerprint(np.ascontiguousarray(s[sample])) == int(meta["fingerprint_s_rows"][-1])
+    draft = np.array([seqs[b][0] for b in range(B)], np.int32)
+    o_nid = np.array([rows[r][0] for r in range(256)], np.int32)
+    o_ml = np.array([rows[r][1] for r in range(256)])
+    o_sec = np.array([rows[r][2] for r in range(256)])
+    o_acc = np.array([seqs[b][1] for b in range(B)], np.int32)
+    g_acc, g_nid, g_ml = run_verify_nvfp4(vh, X, q, s, g, draft, B, k)
+
+    def score_of(r, v):
+        return float(orc.scores_nvfp4(X[r], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0])
+
+    n_exact = check_ids(g_nid, g_ml, o_nid, o_ml, o_sec, score_of, TOL_4BIT)
+    assert n_exact >= 200  # most rows have a clear winner
+    check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
+    sample_rows = np.array([3, 100, 254], np.int32)
+    _, l_nid, l_ml, _ = orc.verify_greedy_nvfp4(X, q, s, g, None, B, k, rows=sample_rows)
+    for r in sample_rows:
+        assert l_nid[r] == o_nid[r] and l_ml[r] == np.float32(o_ml[r])
