@@ -282,6 +282,64 @@ VH_API vh_status spec_verify_greedy_path(const void* hidden, const void* W_full,
                                   int H, int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit,
                                   void* ws, size_t ws_bytes, void* stream, int path);
 
+/* mtp_draft_head_argmax_nvfp4 with an explicit kernel choice (same results
+ * up to fp32 summation order).  VH_PATH_TENSOR: warp-level MMAs in passes of
+ * 16 rows for H = 256 * 2^i <= 4096, else tcgen05 passes of 16 rows for
+ * H % 512 == 0, else VH_ERR_SHAPE.  VH_PATH_CUDA_CORE: the streaming GEMV on
+ * CUDA cores (one pass per 8 rows, fewer for wide H).  VH_PATH_AUTO: the
+ * kernel mtp_draft_head_argmax_nvfp4 runs. */
+VH_API vh_status mtp_draft_head_argmax_nvfp4_path(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                                  float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
+                                                  int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes,
+                                                  void* stream, int path);
+
+/*
+ * Tiled layout of a block-scaled 4-bit head (same NVFP4 format as
+ * mtp_draft_head_argmax_nvfp4, "为什么生产推理我默认 vLLM" §3; NVFP4 candidate
+ * rows in "少读一张大表，草稿路径才真正快起来").  The weights are static, so a
+ * caller converts them once (at load time) with vh_nvfp4_pack and then scores
+ * the tiled copy with the *_nvfp4_packed calls, which read the same bytes per
+ * call as the row-major calls but stream them front to back in the order the
+ * tensor-core fragments need them.
+ *
+ * Layout: rows in blocks of 16 and K in tiles of 256 elements; tile (block
+ * b, tile t) is the 2,304-byte record at byte ((b * H/256) + t) * 2304:
+ *   [h*1024 + L*32, +32) for h = 0, 1 and L = 0..31: the 32 code bytes of row
+ *       16b + L/4 + 8h, elements 256t + 64*(L%4) + [0, 64) (nibble order as in
+ *       the row-major codes);
+ *   [2048 + L*8 + h*4, +4): the 4 E4M3 scales of those elements.
+ * Rows past V are zero.  Size: vh_nvfp4_packed_bytes(V, H) =
+ * ceil(V/16) * 9*H bytes; 0 unless H % 256 == 0.
+ */
+VH_API size_t vh_nvfp4_packed_bytes(int V, int H);
+
+/* Row-major codes Wq [V][H/2] and scales [V][H/16] (device, 16-byte aligned)
+ * -> `packed` (device, 16-byte aligned, at least vh_nvfp4_packed_bytes(V, H)
+ * bytes, else VH_ERR_WORKSPACE).  V >= 1; 256 <= H <= 65536, H % 256 == 0.
+ * Enqueued on `stream`; allocates nothing. */
+VH_API vh_status vh_nvfp4_pack(const uint8_t* Wq, const uint8_t* scales, int V, int H, void* packed,
+                               size_t packed_bytes, void* stream);
+
+/* mtp_draft_head_argmax_nvfp4 over the tiled copy made by vh_nvfp4_pack (the
+ * same ids and max logits up to fp32 summation order).  One pass over the
+ * table per 16 hidden rows on warp-level tensor-core MMAs, the codes streamed
+ * straight into registers.  packed: device, 32-byte aligned.  H % 256 == 0
+ * and H <= 6144 (the f16 copy of 16 hidden rows fits in shared memory), else
+ * VH_ERR_SHAPE.  Other arguments as for mtp_draft_head_argmax_nvfp4. */
+VH_API vh_status mtp_draft_head_argmax_nvfp4_packed(const void* hidden, const void* packed, float tensor_scale,
+                                                    const int32_t* cand_ids, int B, int H, int Vc, int32_t* ids,
+                                                    float* maxlogit, void* ws, size_t ws_bytes, void* stream);
+
+/* spec_verify_greedy_nvfp4 over the tiled copy of the full 4-bit head (V
+ * rows): one pass over the head per 16 hidden rows, the acceptance scan in
+ * the last pass.  Workspace: vh_workspace_bytes(B*(k+1)) (no f16 scratch).
+ * Shapes as for mtp_draft_head_argmax_nvfp4_packed; B, k, V, outputs as for
+ * spec_verify_greedy. */
+VH_API vh_status spec_verify_greedy_nvfp4_packed(const void* hidden, const void* packed, float tensor_scale,
+                                                 const int32_t* draft_ids, int B, int k, int H, int V,
+                                                 int32_t* accept_len, int32_t* next_ids, float* row_maxlogit,
+                                                 void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

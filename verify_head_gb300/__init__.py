@@ -36,6 +36,8 @@ EXPORTS = (
     "mtp_draft_head_argmax_nvfp4", "spec_verify_greedy", "spec_verify_greedy_path",
     "mtp_draft_head_argmax_static_ws", "mtp_draft_head_argmax_gather", "vh_workspace_error_offset",
     "vh_selftest_bounded_wait", "spec_verify_greedy_nvfp4", "vh_verify_nvfp4_workspace_bytes",
+    "mtp_draft_head_argmax_nvfp4_path", "vh_nvfp4_packed_bytes", "vh_nvfp4_pack",
+    "mtp_draft_head_argmax_nvfp4_packed", "spec_verify_greedy_nvfp4_packed",
 )
 
 
@@ -118,6 +120,18 @@ def _declare(L):
     L.mtp_draft_head_argmax_static_ws.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.vh_verify_nvfp4_workspace_bytes.restype = sz
     L.vh_verify_nvfp4_workspace_bytes.argtypes = [i32, i32]
+    L.mtp_draft_head_argmax_nvfp4_path.restype = i32
+    L.mtp_draft_head_argmax_nvfp4_path.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp,
+                                                   i32]
+    L.vh_nvfp4_packed_bytes.restype = sz
+    L.vh_nvfp4_packed_bytes.argtypes = [i32, i32]
+    L.vh_nvfp4_pack.restype = i32
+    L.vh_nvfp4_pack.argtypes = [vp, vp, i32, i32, vp, sz, vp]
+    L.mtp_draft_head_argmax_nvfp4_packed.restype = i32
+    L.mtp_draft_head_argmax_nvfp4_packed.argtypes = [vp, vp, ctypes.c_float, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_greedy_nvfp4_packed.restype = i32
+    L.spec_verify_greedy_nvfp4_packed.argtypes = [vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                                  vp]
     L.spec_verify_greedy_path.restype = i32
     L.spec_verify_greedy_path.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, i32]
 
@@ -228,8 +242,9 @@ def mtp_draft_head_argmax_gather(hidden, W_full, row_ids, ids=None, maxlogit=Non
 
 
 def mtp_draft_head_argmax_nvfp4(hidden, Wq, scales, tensor_scale, cand_ids, ids=None, maxlogit=None, ws=None,
-                                stream=None):
-    """hidden [B,H] bf16, Wq [Vc,H/2] uint8, scales [Vc,H/16] uint8 (E4M3), tensor_scale float."""
+                                stream=None, path: int = VH_PATH_AUTO):
+    """hidden [B,H] bf16, Wq [Vc,H/2] uint8, scales [Vc,H/16] uint8 (E4M3), tensor_scale float.
+    `path` picks the kernel family (VH_PATH_AUTO / VH_PATH_CUDA_CORE / VH_PATH_TENSOR)."""
     torch = _torch()
     _require_cuda(hidden, Wq, scales, cand_ids)
     B, H = hidden.shape
@@ -242,9 +257,9 @@ def mtp_draft_head_argmax_nvfp4(hidden, Wq, scales, tensor_scale, cand_ids, ids=
         maxlogit = torch.empty(B, dtype=torch.float32, device=hidden.device)
     if ws is None:
         ws = workspace(B, hidden.device)
-    st = lib().mtp_draft_head_argmax_nvfp4(_ptr(hidden), _ptr(Wq), _ptr(scales), float(tensor_scale), _ptr(cand_ids),
-                                           B, H, Vc, _ptr(ids), _ptr(maxlogit), _ptr(ws), ws.numel(),
-                                           _stream_ptr(stream))
+    st = lib().mtp_draft_head_argmax_nvfp4_path(_ptr(hidden), _ptr(Wq), _ptr(scales), float(tensor_scale),
+                                                _ptr(cand_ids), B, H, Vc, _ptr(ids), _ptr(maxlogit), _ptr(ws),
+                                                ws.numel(), _stream_ptr(stream), int(path))
     _check(st, "mtp_draft_head_argmax_nvfp4")
     return ids, maxlogit
 
@@ -298,4 +313,75 @@ def spec_verify_greedy_nvfp4(hidden, Wq, scales, tensor_scale, draft_ids, B: int
                                         k, H, V, _ptr(accept_len), _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws),
                                         ws.numel(), _stream_ptr(stream))
     _check(st, "spec_verify_greedy_nvfp4")
+    return accept_len, next_ids, row_maxlogit
+
+
+def vh_nvfp4_packed_bytes(V: int, H: int) -> int:
+    return int(lib().vh_nvfp4_packed_bytes(V, H))
+
+
+def nvfp4_pack(Wq, scales, packed=None, stream=None):
+    """Wq [V,H/2] uint8, scales [V,H/16] uint8 (row-major, CUDA) -> the tiled
+    copy (uint8 CUDA tensor of vh_nvfp4_packed_bytes(V, H) bytes) that the
+    *_nvfp4_packed calls read.  Done once per head (the weights are static)."""
+    torch = _torch()
+    _require_cuda(Wq, scales)
+    V, H = Wq.shape[0], Wq.shape[1] * 2
+    if tuple(scales.shape) != (V, H // 16):
+        raise ValueError("shape mismatch")
+    n = vh_nvfp4_packed_bytes(V, H)
+    if n == 0:
+        raise VHError(VH_ERR_SHAPE, "nvfp4_pack")
+    if packed is None:
+        packed = torch.empty(n, dtype=torch.uint8, device=Wq.device)
+    st = lib().vh_nvfp4_pack(_ptr(Wq), _ptr(scales), V, H, _ptr(packed), packed.numel(), _stream_ptr(stream))
+    _check(st, "vh_nvfp4_pack")
+    return packed
+
+
+def mtp_draft_head_argmax_nvfp4_packed(hidden, packed, tensor_scale, cand_ids, ids=None, maxlogit=None, ws=None,
+                                       stream=None):
+    """hidden [B,H] bf16, packed = nvfp4_pack(...) of the candidate table (Vc = cand_ids.numel() rows)."""
+    torch = _torch()
+    _require_cuda(hidden, packed, cand_ids)
+    B, H = hidden.shape
+    Vc = cand_ids.numel()
+    if packed.numel() < vh_nvfp4_packed_bytes(Vc, H) or hidden.element_size() != 2:
+        raise ValueError("shape mismatch")
+    if ids is None:
+        ids = torch.empty(B, dtype=torch.int32, device=hidden.device)
+    if maxlogit is None:
+        maxlogit = torch.empty(B, dtype=torch.float32, device=hidden.device)
+    if ws is None:
+        ws = workspace(B, hidden.device)
+    st = lib().mtp_draft_head_argmax_nvfp4_packed(_ptr(hidden), _ptr(packed), float(tensor_scale), _ptr(cand_ids), B,
+                                                  H, Vc, _ptr(ids), _ptr(maxlogit), _ptr(ws), ws.numel(),
+                                                  _stream_ptr(stream))
+    _check(st, "mtp_draft_head_argmax_nvfp4_packed")
+    return ids, maxlogit
+
+
+def spec_verify_greedy_nvfp4_packed(hidden, packed, tensor_scale, draft_ids, B: int, k: int, V: int, accept_len=None,
+                                    next_ids=None, row_maxlogit=None, ws=None, stream=None,
+                                    want_maxlogit: bool = True):
+    """hidden [B*(k+1),H] bf16, packed = nvfp4_pack(...) of the full V-row head, draft_ids [B,k] int32
+    -> (accept_len [B], next_ids [B*(k+1)], row_maxlogit or None)."""
+    torch = _torch()
+    _require_cuda(hidden, packed, draft_ids)
+    R, H = hidden.shape
+    if R != B * (k + 1) or draft_ids.numel() != B * k or packed.numel() < vh_nvfp4_packed_bytes(V, H):
+        raise ValueError("shape mismatch")
+    dev = hidden.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_ids is None:
+        next_ids = torch.empty(R, dtype=torch.int32, device=dev)
+    if row_maxlogit is None and want_maxlogit:
+        row_maxlogit = torch.empty(R, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(R, dev)
+    st = lib().spec_verify_greedy_nvfp4_packed(_ptr(hidden), _ptr(packed), float(tensor_scale), _ptr(draft_ids), B, k,
+                                               H, V, _ptr(accept_len), _ptr(next_ids), _ptr(row_maxlogit), _ptr(ws),
+                                               ws.numel(), _stream_ptr(stream))
+    _check(st, "spec_verify_greedy_nvfp4_packed")
     return accept_len, next_ids, row_maxlogit

@@ -15,6 +15,7 @@ constexpr int kGemvRows = 8;   // hidden rows per CUDA-core launch
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
+constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
 constexpr int kMaxDraftB = 256;
 constexpr int kMaxH = 65536;
 
@@ -46,6 +47,12 @@ vh_status check_device() {
 }
 
 vh::Workspace make_ws(void* ws, int /*rows*/) { return vh::ws_view(ws); }
+
+// Shapes the tiled 4-bit kernel takes: H % 256 == 0 and the f16 hidden rows of
+// one 16-row pass (H * 32 bytes) within its shared-memory limit (H <= 6144).
+inline bool packed_shape_ok(int H) {
+    return H >= 256 && H <= kMaxH && H % 256 == 0 && vh::nvfp4_packed_smem(kPackedRows, H) <= vh::nvfp4_packed_max_smem();
+}
 
 vh_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return VH_OK;
@@ -130,12 +137,16 @@ vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_full, c
     return VH_OK;
 }
 
-vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
-                                      float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
-                                      int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
+vh_status mtp_draft_head_argmax_nvfp4_path(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                           float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
+                                           int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream,
+                                           int path) {
     if (!hidden || !Wq || !scales || !cand_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
     if (B < 1 || B > kMaxDraftB || H < 64 || H > kMaxH || H % 64 != 0 || Vc < 1) return VH_ERR_SHAPE;
     if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.0e38f)) return VH_ERR_SHAPE;
+    if (path != VH_PATH_AUTO && path != VH_PATH_CUDA_CORE && path != VH_PATH_TENSOR) return VH_ERR_SHAPE;
+    const bool mma_ok = vh::nvfp4_mma_supported(kMmaFp4Rows, H);
+    if (path == VH_PATH_TENSOR && !mma_ok && H % 512 != 0) return VH_ERR_SHAPE;
     if (!aligned(hidden, 16) || !aligned(Wq, 32) || !aligned(scales, 16) || !aligned(cand_ids, 4) ||
         !aligned(ids, 4) || !aligned(maxlogit, 4) || !aligned(ws, 16))
         return VH_ERR_ALIGN;
@@ -149,9 +160,11 @@ vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, con
     // (H = 256 * 2^i <= 4096).  More rows: tcgen05 in groups of 16 when H is a
     // multiple of the 512-element raw stage (one pass over the head for 16
     // rows beats two 8-row MMA passes), else MMA groups of 8, else CUDA cores.
-    const bool mma_ok = vh::nvfp4_mma_supported(kMmaFp4Rows, H);
-    const bool tc = B > 1 && H % 512 == 0 && !(B <= kMmaFp4Rows && mma_ok);
-    const bool mma = B > 1 && !tc && mma_ok;
+    // VH_PATH_TENSOR takes the same tensor-core kernels for any B;
+    // VH_PATH_CUDA_CORE the GEMV for any B.
+    const bool tensor = path == VH_PATH_TENSOR || (path == VH_PATH_AUTO && B > 1 && (mma_ok || H % 512 == 0));
+    const bool tc = tensor && H % 512 == 0 && !(B <= kMmaFp4Rows && mma_ok);
+    const bool mma = tensor && !tc && mma_ok;
     const int grp = mma ? kMmaFp4Rows : tc ? kTcFp4Rows : gemv_group(H);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
@@ -164,6 +177,13 @@ vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, con
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;
+}
+
+vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
+                                      float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
+                                      int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
+    return mtp_draft_head_argmax_nvfp4_path(hidden, Wq, scales, tensor_scale, cand_ids, B, H, Vc, ids, maxlogit, ws,
+                                            ws_bytes, stream, VH_PATH_AUTO);
 }
 
 vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k,
@@ -278,6 +298,82 @@ vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq, const 
             : tc ? vh::launch_nvfp4_tc(xr, nr, H, Wq, scales, tensor_scale, nullptr, V, w, next_ids + r0, ml, s, tail)
                  : vh::launch_gemv_nvfp4(xr, nr, H, Wq, scales, tensor_scale, nullptr, V, w, next_ids + r0, ml, s,
                                          tail);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
+size_t vh_nvfp4_packed_bytes(int V, int H) { return vh::nvfp4_packed_bytes(V, H); }
+
+vh_status vh_nvfp4_pack(const uint8_t* Wq, const uint8_t* scales, int V, int H, void* packed, size_t packed_bytes,
+                        void* stream) {
+    if (!Wq || !scales || !packed) return VH_ERR_NULL;
+    if (V < 1 || H < 256 || H > kMaxH || H % 256 != 0) return VH_ERR_SHAPE;
+    if (!aligned(Wq, 16) || !aligned(scales, 16) || !aligned(packed, 16)) return VH_ERR_ALIGN;
+    if (packed_bytes < vh::nvfp4_packed_bytes(V, H)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    return launch_status(vh::launch_nvfp4_pack(Wq, scales, V, H, static_cast<uint8_t*>(packed),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+vh_status mtp_draft_head_argmax_nvfp4_packed(const void* hidden, const void* packed, float tensor_scale,
+                                             const int32_t* cand_ids, int B, int H, int Vc, int32_t* ids,
+                                             float* maxlogit, void* ws, size_t ws_bytes, void* stream) {
+    if (!hidden || !packed || !cand_ids || !ids || !maxlogit || !ws) return VH_ERR_NULL;
+    if (B < 1 || B > kMaxDraftB || !packed_shape_ok(H) || Vc < 1) return VH_ERR_SHAPE;
+    if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.0e38f)) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(packed, 32) || !aligned(cand_ids, 4) || !aligned(ids, 4) ||
+        !aligned(maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    if (ws_bytes < vh_workspace_bytes(B)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, B);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const uint8_t* P = static_cast<const uint8_t*>(packed);
+    for (int b0 = 0; b0 < B; b0 += kPackedRows) {
+        const int nb = std::min(kPackedRows, B - b0);
+        cudaError_t e = vh::launch_nvfp4_packed(x + (size_t)b0 * H, nb, H, P, tensor_scale, cand_ids, Vc, w, ids + b0,
+                                                maxlogit + b0, s);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return VH_OK;
+}
+
+vh_status spec_verify_greedy_nvfp4_packed(const void* hidden, const void* packed, float tensor_scale,
+                                          const int32_t* draft_ids, int B, int k, int H, int V, int32_t* accept_len,
+                                          int32_t* next_ids, float* row_maxlogit, void* ws, size_t ws_bytes,
+                                          void* stream) {
+    if (!hidden || !packed || !draft_ids || !accept_len || !next_ids || !ws) return VH_ERR_NULL;
+    if (B < 1 || k < 1 || k > 15 || !packed_shape_ok(H) || V < 1) return VH_ERR_SHAPE;
+    if ((long long)B * (k + 1) > 65536) return VH_ERR_SHAPE;
+    if (!(tensor_scale > 0.0f) || !(tensor_scale < 3.0e38f)) return VH_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(packed, 32) || !aligned(draft_ids, 4) || !aligned(accept_len, 4) ||
+        !aligned(next_ids, 4) || !aligned(row_maxlogit, 4) || !aligned(ws, 16))
+        return VH_ERR_ALIGN;
+    const int R = B * (k + 1);
+    if (ws_bytes < vh_workspace_bytes(R)) return VH_ERR_WORKSPACE;
+    vh_status st = check_device();
+    if (st != VH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const vh::Workspace w = make_ws(ws, R);
+    const uint16_t* x = static_cast<const uint16_t*>(hidden);
+    const uint8_t* P = static_cast<const uint8_t*>(packed);
+    for (int r0 = 0; r0 < R; r0 += kPackedRows) {
+        const int nr = std::min(kPackedRows, R - r0);
+        vh::AcceptTail tail;
+        if (r0 + nr == R) {  // the final group also runs the acceptance scan
+            tail.draft = draft_ids;
+            tail.next_ids = next_ids;
+            tail.accept_len = accept_len;
+            tail.B = B;
+            tail.k = k;
+        }
+        float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
+        cudaError_t e = vh::launch_nvfp4_packed(x + (size_t)r0 * H, nr, H, P, tensor_scale, nullptr, V, w,
+                                                next_ids + r0, ml, s, tail);
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;

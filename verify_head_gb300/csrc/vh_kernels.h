@@ -48,6 +48,22 @@ cudaError_t launch_nvfp4_mma(const uint16_t* x, int nb, int H, const uint8_t* Wq
                              const int32_t* cand, int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
                              const AcceptTail& tail = AcceptTail{});
 
+// Tiled ("packed") layout of a block-scaled 4-bit head: records of 16 rows x
+// 256 elements (2,048 code bytes in MMA-fragment order + 256 scale bytes).
+// nvfp4_packed_bytes: size for V rows of width H (0 unless H % 256 == 0).
+size_t nvfp4_packed_bytes(long long V, int H);
+// Shared memory of launch_nvfp4_packed for nb rows of width H, and its limit.
+size_t nvfp4_packed_smem(int nb, int H);
+size_t nvfp4_packed_max_smem();
+// Row-major codes [V][H/2] + scales [V][H/16] -> the tiled layout.
+cudaError_t launch_nvfp4_pack(const uint8_t* Wq, const uint8_t* scales, int V, int H, uint8_t* packed, cudaStream_t s);
+// Block-scaled 4-bit head in the tiled layout, nb <= 16 hidden rows on
+// warp-level MMAs, one pass over the table.  Returns cudaErrorNotSupported
+// for other shapes.
+cudaError_t launch_nvfp4_packed(const uint16_t* x, int nb, int H, const uint8_t* packed, float g, const int32_t* cand,
+                                int Vc, Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s,
+                                const AcceptTail& tail = AcceptTail{});
+
 // tcgen05 skinny GEMM + per-row argmax + acceptance scan for R <= 256 hidden
 // rows (H % 64 == 0).  Returns cudaErrorNotSupported when the shape does not
 // fit the kernel.
