@@ -74,10 +74,14 @@ def dist_env():
 # clocks during the timed region
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every 20 ms from before the warm-up
+    to the end of the run; mark() brackets the timed region of the headline."""
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.start = 0
+        self.region = None  # (start, end) byte offsets of the timed region in the sample file
         # the raw samples (the JSON line carries their summary); VH_BENCH_LOG_DIR overrides the location
         log_dir = os.environ.get("VH_BENCH_LOG_DIR") or tempfile.gettempdir()
         self.path = os.path.join(log_dir, f"vh_clocks_rank{index}.csv")
@@ -92,8 +96,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
-            # wait (at most 3 s) for the sampler's first line, then count only what follows:
-            # the samples that fall inside the timed region
+            # wait (at most 3 s) for the sampler's first line, then count what follows
             t0 = time.time()
             while time.time() - t0 < 3.0 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
                 time.sleep(0.01)
@@ -101,6 +104,13 @@ class ClockSampler:
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def mark(self, begin: bool):
+        if self.proc is None:
+            return
+        self.f.flush()
+        off = os.path.getsize(self.path)
+        self.region = (off, None) if begin else (self.region[0] if self.region else self.start, off)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -111,36 +121,47 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
-        if self.proc is None:
-            return None
+    @staticmethod
+    def _parse(lines):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return sm, mx, reasons
+
+    def summary(self):
+        """Median SM clock, the maximum, and every throttle reason seen over
+        the whole run (warm-up, timed chains and the other workloads); the
+        headline's timed region is also given on its own when it holds
+        samples (the driver's short runs time about 3 ms)."""
+        if self.proc is None:
+            return None
         try:
             with open(self.path) as f:
                 text = f.read()
-            lines = text[self.start:].splitlines()
-            window = "timed region"
-            if not any(len(x.split(",")) >= 9 for x in lines):  # region shorter than the sampling interval
-                lines, window = text.splitlines(), "around the timed region (region shorter than one sample)"
-            for line in lines:
-                p = [x.strip() for x in line.split(",")]
-                if len(p) < 9:
-                    continue
-                try:
-                    sm.append(float(p[1]))
-                    mx.append(float(p[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, p[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
         except OSError:
             return None
+        sm, mx, reasons = self._parse(text[self.start:].splitlines())
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "window": window}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm), "window": "whole run: warm-up, timed chains and every other workload",
+               "sample_interval_ms": 20}
+        if self.region and self.region[1] is not None:
+            r_sm, _, r_reasons = self._parse(text[self.region[0]:self.region[1]].splitlines())
+            out["timed_region"] = ({"sm_mhz": statistics.median(r_sm), "samples": len(r_sm),
+                                    "reasons": sorted(r_reasons)} if r_sm else {"samples": 0})
+        return out
 
 
 # ----------------------------------------------------------------------------
@@ -270,6 +291,8 @@ def run_ours(args):
 
     bytes_per_call = case.Vc * case.H * 2 + case.Vc * 4 + case.B * case.H * 2
 
+    sampler = ClockSampler(local)
+    sampler.__enter__()  # clocks from the warm-up to the end of the run
     for _ in range(max(3, args.warmup)):
         for i in range(3):
             timer.flush()
@@ -278,19 +301,19 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    with sampler:
-        evs = []
-        for _ in range(args.steps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            timer.flush()
-            a.record()
-            for i in range(3):  # one MTP3 draft chain: three dependent-launch calls back to back
-                call(i)
-            b.record()
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        per_step = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    sampler.mark(True)
+    evs = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        timer.flush()
+        a.record()
+        for i in range(3):  # one MTP3 draft chain: three dependent-launch calls back to back
+            call(i)
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    per_step = [a.elapsed_time(b) * 1e3 for a, b in evs]
     # warm extra: the same chain with no L2 flush in between (the 268 MB table is twice
     # the L2, so most of it still streams from HBM); reported beside the value, never as it
     warm_evs = []
@@ -381,6 +404,7 @@ def run_ours(args):
     extra = {}
     if rank == 0 and not args.skip_extra and args.workload == "all":
         extra = measure_extra(torch, vh, synth, timer, peaks, load_verify_golden)
+    sampler.__exit__(None, None, None)
 
     cpu, parity = None, None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -426,16 +450,60 @@ def run_ours(args):
         "parity": parity,
     }
     line.update(extra)
+    line["summary"] = summarize(line)  # last key: a compact digest of every workload
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
+def summarize(line):
+    """One short entry per workload (config 1 tiny, 2 draft, 3 sweep, 4 verify,
+    5 4-bit draft; the gather, 4-bit verify and end-to-end figures), so that a
+    reader of the end of the line sees every result: [us per call or round,
+    fraction of the measured HBM roofline] unless named otherwise."""
+    def g(d, *ks):
+        for k in ks:
+            if not isinstance(d, dict) or k not in d:
+                return None
+            d = d[k]
+        return d
+
+    def pair(d, us_key="median_us", frac_key="hbm_frac"):
+        return None if not isinstance(d, dict) else [d.get(us_key), d.get(frac_key)]
+
+    s = {"draft_65536x2048": {"steps_per_s": line["value"], "us": g(line, "draft_call_us", "mean_us"),
+                              "hbm_frac": g(line, "roofline", "frac")},
+         "e2e_steps_per_s": g(line, "e2e", "value")}
+    t = line.get("tiny")
+    if t:
+        s["tiny_4096x256"] = {"draft_us": g(t, "draft_call_us", "median_us"),
+                              "verify_us": g(t, "verify_call_us", "median_us"),
+                              "ids": t.get("draft_ids_equal_oracle"), "verify_ids": t.get("verify_next_ids_equal_oracle")}
+    if line.get("sweep"):
+        s["sweep"] = {k: pair(v, "mean_us") for k, v in line["sweep"].items()}
+    v = line.get("verify")
+    if v:
+        s["verify_256x248320"] = {"rounds_per_s": v.get("rounds_per_s"), "us": v.get("median_us"),
+                                  "hbm_frac": v.get("hbm_frac"), "tensor_frac_burst": v.get("tensor_frac_burst"),
+                                  "tensor_frac_sustained": v.get("tensor_frac_sustained")}
+    if line.get("gather"):
+        s["gather"] = pair(line["gather"], "mean_us")
+    nv = line.get("nvfp4")
+    if nv:
+        s["nvfp4_65536x4096"] = {**{k: pair(v, "mean_us") for k, v in nv.items() if k.startswith("B")},
+                                 **{"row_major_" + k: pair(v, "mean_us") for k, v in nv.get("row_major", {}).items()}}
+    if line.get("verify_nvfp4"):
+        s["verify_nvfp4"] = {k.replace("head_", "").replace("full_head_", "full_"): pair(v)
+                             for k, v in line["verify_nvfp4"].items()}
+    s["peaks"] = g(line, "roofline", "peak_source")
+    return s
+
+
 def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"):
     dev = torch.device("cuda")
     out = {}
-    if only == "tiny":
+    if only in ("all", "tiny"):
         out["tiny"] = measure_tiny(torch, vh, synth, timer)
     if only in ("all", "verify"):
         out.update(measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=(only == "verify")))
@@ -518,6 +586,7 @@ def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core
             "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
             "tflops": round(flops / (med * 1e-6) / 1e12, 1),
             "tensor_frac_burst": round(flops / (med * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+            "tensor_frac_sustained": round(flops / (med * 1e-6) / 1e12 / peaks["bf16_tflops_sustained"], 4),
             "accept_hist": np.bincount(a, minlength=4).tolist(), "mean_accept": round(float(a.mean()), 4),
             "matches_stored_oracle_ids": int((nid.cpu().numpy() == gold["next_ids"]).sum()),
             "gpu_launches_per_round": 1 if path == vh.VH_PATH_TENSOR else 32,
@@ -678,6 +747,20 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
         "workload": "4 seqs x 4 rows x 4096 bf16 vs 65,536 x 4096 4-bit head", "kernel": "k_nvfp4_tc",
         "rounds_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
         "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    # the same 16 and 4 rows against the tiled copy of the head
+    P = vh.nvfp4_pack(q, s)
+    for R in (16, 4):
+        Xr, dr = X[:R].contiguous(), d[:R // 4].contiguous()
+        wsr = vh.workspace(R)
+        us = timer.time_calls(lambda: vh.spec_verify_greedy_nvfp4_packed(Xr, P, c.g, dr, R // 4, 3, 65_536, ws=wsr), 20)
+        med = statistics.median(us)
+        nbytes = c.q.nbytes + c.s.nbytes + R * 4096 * 2
+        out[f"tiled_65536x4096_{R}_rows"] = {
+            "workload": f"{R // 4} seqs x 4 rows x 4096 bf16 vs the tiled 65,536 x 4096 4-bit head",
+            "kernel": "k_nvfp4_packed<%d>" % (2 if R > 8 else 1),
+            "rounds_per_s": round(1e6 / med, 1), **stats(us), "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    del P
     # 4 rows (one MTP3 sequence) vs the same head
     X4, d1 = X[:4].contiguous(), d[:1].contiguous()
     ws = vh.verify_nvfp4_workspace(4, 4096)
@@ -692,37 +775,57 @@ def measure_verify_nvfp4(torch, vh, synth, timer, peaks):
 
 
 def measure_nvfp4(torch, vh, synth, timer, peaks):
-    """4-bit draft head 65,536 x 4096 at B = 1 and B = 8: three draft steps
-    per chain as in the bench step (per call = chain / 3), and single calls."""
+    """4-bit draft head 65,536 x 4096 at B = 1, 8 and 16: three draft steps
+    per chain as in the bench step (per call = chain / 3), and single calls.
+    The head is converted once to the tiled layout (vh_nvfp4_pack, as a model
+    loader would) and scored with mtp_draft_head_argmax_nvfp4_packed, which
+    reads the same bytes per call; the row-major call is timed beside it."""
     dev = torch.device("cuda")
 
     def t_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    nv = {}
-    for B in (1, 8):
-        c = synth.nvfp4_case(Vc=65_536, H=4096, B=B, steps=3, seed=5)
-        q = torch.from_numpy(c.q).to(dev)
-        s = torch.from_numpy(c.s).to(dev)
-        cc = torch.from_numpy(c.cand_ids).to(dev)
-        xs = [t_bf16(h) for h in c.hidden]
+    nv, rm = {}, {}
+    c = synth.nvfp4_case(Vc=65_536, H=4096, B=16, steps=3, seed=5)
+    q = torch.from_numpy(c.q).to(dev)
+    s = torch.from_numpy(c.s).to(dev)
+    cc = torch.from_numpy(c.cand_ids).to(dev)
+    P = vh.nvfp4_pack(q, s)
+    for B in (1, 8, 16):
+        xs = [t_bf16(h[:B]) for h in c.hidden]
         wsb = vh.workspace(B)
         ids = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(3)]
         mls = [torch.empty(B, dtype=torch.float32, device=dev) for _ in range(3)]
-
-        def chain():
-            for k in range(3):
-                vh.mtp_draft_head_argmax_nvfp4(xs[k], q, s, c.g, cc, ids=ids[k], maxlogit=mls[k], ws=wsb)
-
-        us = [t / 3 for t in timer.time_calls(chain, 20)]
-        single = timer.time_calls(lambda: vh.mtp_draft_head_argmax_nvfp4(xs[0], q, s, c.g, cc, ws=wsb), 20)
-        mean = statistics.mean(us)
         nbytes = c.q.nbytes + c.s.nbytes + 65_536 * 4 + B * 4096 * 2
-        nv[f"B{B}"] = {"timing": "3-call chains, per call", "steps_per_s": round(1e6 / mean, 1), **stats(us),
-                       "hbm_gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
-                       "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                       "single_call_us": stats(single),
-                       "kernel": "k_gemv_nvfp4_xs" if B == 1 else "k_nvfp4_mma"}
+        for layout in ("tiled", "row_major"):
+            if layout == "row_major" and B == 16:
+                continue
+
+            def one(k, layout=layout):
+                if layout == "tiled":
+                    vh.mtp_draft_head_argmax_nvfp4_packed(xs[k], P, c.g, cc, ids=ids[k], maxlogit=mls[k], ws=wsb)
+                else:
+                    vh.mtp_draft_head_argmax_nvfp4(xs[k], q, s, c.g, cc, ids=ids[k], maxlogit=mls[k], ws=wsb)
+
+            def chain():
+                for k in range(3):
+                    one(k)
+
+            us = [t / 3 for t in timer.time_calls(chain, 20)]
+            single = timer.time_calls(lambda: one(0), 20)
+            mean = statistics.mean(us)
+            entry = {"timing": "3-call chains, per call", "steps_per_s": round(1e6 / mean, 1), **stats(us),
+                     "hbm_gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
+                     "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "single_call_us": stats(single),
+                     "kernel": ("k_nvfp4_packed<%d> (tiled layout, warp-level MMAs)" % (1 if B <= 8 else 2))
+                     if layout == "tiled" else ("k_gemv_nvfp4_xs" if B == 1 else "k_nvfp4_mma")}
+            if layout == "tiled":
+                entry["algorithmic_bytes_per_launch"] = nbytes
+                nv[f"B{B}"] = entry
+            else:
+                rm[f"B{B}"] = entry
+    nv["row_major"] = rm
     return nv
 
 def run_single(args):
