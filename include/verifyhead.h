@@ -125,6 +125,11 @@ VH_API vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_
 /*
  * Restricted-vocabulary draft head, block-scaled 4-bit weights (NVFP4).
  *
+ * Source: "为什么生产推理我默认 vLLM" §3 (NVFP4: 4-bit weights with scale
+ * factors) and "少读一张大表，草稿路径才真正快起来" (the upstream candidate
+ * head keeps its candidate rows in NVFP4; the draft returns a global id from
+ * the candidate table).
+ *
  * Weight (c, h) = e2m1(code) * e4m3(scales[c][h/16]) * tensor_scale, where
  * code is the low nibble of Wq[c][h/2] for even h and the high nibble for
  * odd h; E2M1 = sign, 2 exponent bits (bias 1), 1 mantissa bit (magnitudes
@@ -137,7 +142,8 @@ VH_API vh_status mtp_draft_head_argmax_gather(const void* hidden, const void* W_
  * 4096 in one pass of warp-level MMAs fed from registers; otherwise tcgen05
  * passes of 16 rows when H % 512 == 0, warp-level MMA passes of 8 rows when
  * H == 256, else CUDA-core passes of 8 rows.  Every pass reads the whole
- * table once.
+ * table once.  (A head converted once with vh_nvfp4_pack is scored faster by
+ * mtp_draft_head_argmax_nvfp4_packed, below.)
  *
  *  hidden        device, bf16 [B][H], 16-byte aligned
  *  Wq            device, uint8 [Vc][H/2], 32-byte aligned
@@ -153,6 +159,14 @@ VH_API vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* 
 
 /*
  * Greedy speculative verification over the full output head.
+ *
+ * Source: "少读一张大表，草稿路径才真正快起来" (the draft path scores a small
+ * candidate table while the target model keeps the full 248,320-row head and
+ * verifies the draft tokens) and "长上下文推理优化" §5 (the MTP loop: draft
+ * proposals, target verification, several tokens accepted per step;
+ * acceptance rate and mean accepted length as its metrics).  The greedy rule
+ * below is the plainest reading of "the target verifies": a draft token is
+ * accepted while it equals the target's own argmax at that position.
  *
  * Row r = b*(k+1) + j of `hidden` is the target model's hidden state for
  * sequence b after its context plus draft tokens 0..j-1 (j = 0 is the
@@ -204,7 +218,9 @@ VH_API vh_status spec_verify_greedy(const void* hidden, const void* W_full, cons
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.
+ * first call before any stream capture.  The cached address belongs to that
+ * device's context: after cudaDeviceReset it may be stale, so a device reset
+ * in the process is not supported for this entry point.
  *
  * Arguments as for mtp_draft_head_argmax, without ws / ws_bytes.
  */
@@ -245,6 +261,9 @@ VH_API size_t vh_verify_nvfp4_workspace_bytes(int rows, int H);
  * NVFP4 format of mtp_draft_head_argmax_nvfp4, rows = the V vocabulary
  * entries).  Rows, next_ids, row_maxlogit and accept_len are defined as for
  * spec_verify_greedy, with W_full replaced by the decoded 4-bit head.
+ * Source: the verification of "少读一张大表，草稿路径才真正快起来" and
+ * "长上下文推理优化" §5 (as for spec_verify_greedy) over the NVFP4 weights of
+ * "为什么生产推理我默认 vLLM" §3.
  *
  * Kernels: up to 8 rows in one pass of warp-level MMAs fed from registers
  * (H = 256 * 2^i <= 4096); up to 16 rows in one tcgen05 pass with N = 16
@@ -277,17 +296,20 @@ typedef enum {
 } vh_path;
 
 /* spec_verify_greedy with an explicit kernel choice (same results up to fp32
- * summation order). */
+ * summation order); the same passages define it. */
 VH_API vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k,
                                   int H, int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit,
                                   void* ws, size_t ws_bytes, void* stream, int path);
 
 /* mtp_draft_head_argmax_nvfp4 with an explicit kernel choice (same results
- * up to fp32 summation order).  VH_PATH_TENSOR: warp-level MMAs in passes of
- * 16 rows for H = 256 * 2^i <= 4096, else tcgen05 passes of 16 rows for
- * H % 512 == 0, else VH_ERR_SHAPE.  VH_PATH_CUDA_CORE: the streaming GEMV on
- * CUDA cores (one pass per 8 rows, fewer for wide H).  VH_PATH_AUTO: the
- * kernel mtp_draft_head_argmax_nvfp4 runs. */
+ * up to fp32 summation order; the same passages define it).  VH_PATH_TENSOR:
+ * the tensor-core kernels that mtp_draft_head_argmax_nvfp4 takes for B > 1,
+ * for any B (warp-level MMAs in passes of 8 rows for H = 256 * 2^i <= 4096
+ * and B <= 8, else tcgen05 passes of 16 rows when H % 512 == 0, else
+ * warp-level MMA passes of 8 rows; VH_ERR_SHAPE when neither applies).
+ * VH_PATH_CUDA_CORE: the streaming GEMV on CUDA cores (one pass per 8 rows,
+ * fewer for wide H).  VH_PATH_AUTO: the kernel mtp_draft_head_argmax_nvfp4
+ * runs. */
 VH_API vh_status mtp_draft_head_argmax_nvfp4_path(const void* hidden, const uint8_t* Wq, const uint8_t* scales,
                                                   float tensor_scale, const int32_t* cand_ids, int B, int H, int Vc,
                                                   int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes,

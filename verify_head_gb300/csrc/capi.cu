@@ -11,23 +11,14 @@
 
 namespace {
 
-constexpr int kGemvRows = 8;   // hidden rows per CUDA-core launch
+using vh::gemv_group;
+using vh::kMaxDraftB;
+using vh::kMaxH;
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
-constexpr int kMaxDraftB = 256;
-constexpr int kMaxH = 65536;
-
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
-// Hidden rows per CUDA-core launch: up to 8, fewer when the staged hidden
-// rows (rows x H bf16 in shared memory) would exceed 128 KiB.
-inline int gemv_group(int H) {
-    int g = kGemvRows;
-    while (g > 1 && (size_t)g * H * 2 > 131072) g /= 2;
-    return g;
-}
 
 vh_status check_device() {
     static std::atomic<int> ok_cache[64] = {};  // 1: device already checked

@@ -15,7 +15,9 @@
 // per call.  Host code only ever sees a host-side stand-in under that name,
 // so the device address is looked up with cudaGetSymbolAddress once per
 // device (on that device's first call, with the device current) and passed
-// to the kernel.
+// to the kernel.  The cached address belongs to the context of that first
+// call: after cudaDeviceReset the module is loaded again and the address may
+// change, so this entry point does not support a device reset in the process.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,7 +29,7 @@
 
 namespace {
 
-constexpr int kStaticMaxRows = 256;
+constexpr int kStaticMaxRows = vh::kMaxDraftB;
 constexpr size_t kStaticScratchBytes = 4096;
 static_assert(vh::ws_total_bytes(kStaticMaxRows) <= kStaticScratchBytes, "static scratch too small");
 
@@ -66,7 +68,7 @@ extern "C" {
 vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand, const int32_t* cand_ids, int B,
                                           int H, int Vc, int32_t* ids, float* maxlogit, void* stream) {
     if (!hidden || !W_cand || !cand_ids || !ids || !maxlogit) return VH_ERR_NULL;
-    if (B < 1 || H < 16 || H > 65536 || H % 16 != 0 || Vc < 1) return VH_ERR_SHAPE;
+    if (B < 1 || H < 16 || H > vh::kMaxH || H % 16 != 0 || Vc < 1) return VH_ERR_SHAPE;
     if (B > kStaticMaxRows) return VH_ERR_WORKSPACE;  // more rows than the fixed scratch holds
     if (!aligned(hidden, 16) || !aligned(W_cand, 32) || !aligned(cand_ids, 4) || !aligned(ids, 4) ||
         !aligned(maxlogit, 4))
@@ -88,8 +90,7 @@ vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand
         return VH_ERR_LAUNCH;
     }
     const vh::Workspace w = vh::ws_view(scratch);
-    int grp = 8;
-    while (grp > 1 && (size_t)grp * H * 2 > 131072) grp /= 2;
+    const int grp = vh::gemv_group(H);  // the same launch groups as mtp_draft_head_argmax
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);

@@ -7,6 +7,19 @@
 
 namespace vh {
 
+// Limits of the C ABI shared by every entry point.
+constexpr int kMaxDraftB = 256;  // hidden rows per draft call
+constexpr int kMaxH = 65536;     // hidden width
+constexpr int kGemvRows = 8;     // hidden rows per CUDA-core launch
+
+// Hidden rows per CUDA-core launch for width H: up to kGemvRows, fewer when
+// the staged hidden rows (rows x H bf16 in shared memory) would exceed 128 KiB.
+inline int gemv_group(int H) {
+    int g = kGemvRows;
+    while (g > 1 && (size_t)g * H * 2 > 131072) g /= 2;
+    return g;
+}
+
 // Optional acceptance scan run by the last CTA of a launch, after the group's
 // argmax ids are written: accept_len[b] = leading j < k with
 // next_ids[b*(k+1)+j] == draft[b*k+j], over all B sequences.
