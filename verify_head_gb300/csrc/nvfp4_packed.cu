@@ -33,6 +33,9 @@
 // acc * g * 2^-k_n.
 #include <algorithm>
 #include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "vh_kernels.h"
 #include "vh_ptx.cuh"
@@ -40,8 +43,8 @@
 namespace vh {
 namespace fp4p {
 
-constexpr int kWarpsP = 16;
-constexpr int kThreadsP = kWarpsP * 32;
+constexpr int kWarpsNT1 = 16;    // warps per CTA with one n8 tile (up to 8 hidden rows); 16 / kWarpsNT1 CTAs per SM
+constexpr int kWarpsNT2 = 16;    // warps per CTA with two n8 tiles (9..16 hidden rows)
 constexpr int kTileK = 256;      // elements of K per tile
 constexpr int kTileBytes = 2304;  // 2,048 code bytes + 256 scale bytes
 constexpr int kBlkRows = 16;     // head rows per block (MMA M)
@@ -202,8 +205,9 @@ __device__ __forceinline__ void block_argmax(const float4 (&s)[NT], int row0, in
 // cut by a range boundary is finished after all warps are done: each warp
 // leaves its partial sums of its first and last block in shared memory, and
 // the warp that holds the block's first tile adds the pieces in warp order.
-template <int NT>
-__global__ void __launch_bounds__(kThreadsP, 1) k_nvfp4_packed(const Args a) {
+template <int NT, int kWarpsP>
+__global__ void __launch_bounds__(kWarpsP * 32, 16 / kWarpsP) k_nvfp4_packed(const Args a) {
+    constexpr int kThreadsP = kWarpsP * 32;
     constexpr int N = 8 * NT;
     constexpr int CH = NT == 1 ? 2 : 1;  // independent accumulation chains per n8 tile
     constexpr int D = kDepth;
@@ -467,6 +471,25 @@ __global__ void k_nvfp4_pack(const uint8_t* __restrict__ Wq, const uint8_t* __re
     *reinterpret_cast<uint32_t*>(r + 2048 + L * 8 + h * 4) = s;
 }
 
+// Resident CTAs per SM of a launch shape, cached per (kernel, threads, shared memory, device).
+static cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int& per_sm) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, size_t, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const auto key = std::make_tuple(kernel, threads, smem, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+        per_sm = it->second;
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    cache[key] = per_sm;
+    return cudaSuccess;
+}
+
 }  // namespace fp4p
 
 size_t nvfp4_packed_bytes(long long V, int H) {
@@ -510,13 +533,18 @@ cudaError_t launch_nvfp4_packed(const uint16_t* x, int nb, int H, const uint8_t*
     a.ids = ids;
     a.maxlogit = maxlogit;
     a.tail = tail;
-    auto kernel = nb <= 8 ? k_nvfp4_packed<1> : k_nvfp4_packed<2>;
+    auto kernel = nb <= 8 ? k_nvfp4_packed<1, kWarpsNT1> : k_nvfp4_packed<2, kWarpsNT2>;
+    const int threads = 32 * (nb <= 8 ? kWarpsNT1 : kWarpsNT2);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int grid = std::max(1, std::min(sm_count(), a.n_blk));
+    int per_sm = 0;
+    e = resident_ctas(reinterpret_cast<const void*>(kernel), threads, smem, per_sm);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    const int grid = std::max(1, std::min(sm_count() * per_sm, a.n_blk));  // one resident wave
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreadsP);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
