@@ -43,13 +43,17 @@
 namespace vh {
 namespace fp4p {
 
-constexpr int kWarpsNT1 = 16;    // warps per CTA with one n8 tile (up to 8 hidden rows); 16 / kWarpsNT1 CTAs per SM
+constexpr int kWarpsNT1 = 16;    // warps per CTA with one n8 tile (up to 8 hidden rows)
 constexpr int kWarpsNT2 = 16;    // warps per CTA with two n8 tiles (9..16 hidden rows)
 constexpr int kTileK = 256;      // elements of K per tile
 constexpr int kTileBytes = 2304;  // 2,048 code bytes + 256 scale bytes
 constexpr int kBlkRows = 16;     // head rows per block (MMA M)
-constexpr int kDepth = 3;        // tiles in flight per warp in registers
-constexpr int kPrefetch = 1;     // tiles prefetched into L2 beyond those loaded into registers
+// tiles in flight per warp in registers, and tiles prefetched into L2 beyond them, by n8 tile count
+// (the two-tile kernel holds twice the B fragments and accumulators, so fewer tiles in registers)
+constexpr int kDepthNT1 = 3;
+constexpr int kPrefetchNT1 = 1;
+constexpr int kDepthNT2 = 1;
+constexpr int kPrefetchNT2 = 2;
 // dynamic shared memory (the f16 hidden rows) at most: with the static arrays
 // (up to 33 KB) within the 227 KB a CTA may use
 constexpr size_t kMaxDynSmem = 192 * 1024;
@@ -206,11 +210,12 @@ __device__ __forceinline__ void block_argmax(const float4 (&s)[NT], int row0, in
 // leaves its partial sums of its first and last block in shared memory, and
 // the warp that holds the block's first tile adds the pieces in warp order.
 template <int NT, int kWarpsP>
-__global__ void __launch_bounds__(kWarpsP * 32, 16 / kWarpsP) k_nvfp4_packed(const Args a) {
+__global__ void __launch_bounds__(kWarpsP * 32, 1) k_nvfp4_packed(const Args a) {
     constexpr int kThreadsP = kWarpsP * 32;
     constexpr int N = 8 * NT;
     constexpr int CH = NT == 1 ? 2 : 1;  // independent accumulation chains per n8 tile
-    constexpr int D = kDepth;
+    constexpr int D = NT == 1 ? kDepthNT1 : kDepthNT2;
+    constexpr int kPrefetch = NT == 1 ? kPrefetchNT1 : kPrefetchNT2;
     extern __shared__ __align__(16) uint8_t xfrag[];  // [H/16 MMAs][NT][32 lanes][8 B]
     __shared__ float4 cut[kWarpsP][2][NT][32];         // partial sums of cut blocks
     __shared__ unsigned long long merge[N];
