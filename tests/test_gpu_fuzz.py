@@ -1,7 +1,7 @@
 """Seeded random shapes through every entry point against the oracle: batch
 sizes, widths (every allowed multiple), table sizes, k and gathered id lists
 drawn at random, so that kernel selection boundaries, ragged tails and group
-splits are hit in combinations no hand-picked list covers (46 cases by
+splits are hit in combinations no hand-picked list covers (54 cases by
 default; VH_FUZZ_SCALE multiplies every family)."""
 import os
 
@@ -179,3 +179,39 @@ def test_fuzz_nvfp4_mma(vh, orc, syn, case):
     check_ids(nid, vml.cpu().numpy(), v_nid, v_ml, v_sec,
               lambda r, v: float(orc.scores_nvfp4(X[r], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0]), TOL_4BIT)
     np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid, draft, Bv, k))
+
+
+@pytest.mark.parametrize("case", range(8 * SCALE))
+def test_fuzz_nvfp4_tiled(vh, orc, syn, case):
+    """The tiled 4-bit layout: random B (1..40, several 16-row passes), width
+    (every multiple of 256 up to 6144), table size and, every other case, a
+    verify with its acceptance scan instead of a draft."""
+    import torch
+    rng = np.random.default_rng(1700 + case)
+    H = 256 * int(rng.integers(1, 25))
+    q_rows = _rows_for(rng, MAC_BUDGET // 2, 16 * H, hi=20_000)
+    q, s, g = syn.nvfp4_quantize(syn.normal_f32(7000 + case, 6, (q_rows, H), 0.02))
+    P = vh.nvfp4_pack(to_torch(q), to_torch(s))
+    if case % 2 == 0:
+        B = int(rng.choice([1, 2, 7, 8, 9, 16, 17, 33, 40]))
+        cand = syn.sorted_subset(7000 + case, 2, 248_320, q_rows)
+        x = syn.normal_bf16(8000 + case, 3, (B, H), 1.0)
+        ids, ml = vh.mtp_draft_head_argmax_nvfp4_packed(to_torch_bf16(x), P, g, to_torch(cand))
+        torch.cuda.synchronize()
+        o_ids, o_ml, o_sec = orc.draft_argmax_nvfp4(x, q, s, g, cand)
+
+        def score_of(r, gid):
+            c = int(np.searchsorted(cand, gid))
+            return float(orc.scores_nvfp4(x[r], q[c:c + 1], s[c:c + 1], g, nthreads=1)[0])
+
+        check_ids(ids.cpu().numpy(), ml.cpu().numpy(), o_ids, o_ml, o_sec, score_of, TOL_4BIT)
+    else:
+        B, k = int(rng.choice([1, 2, 4, 5, 9])), int(rng.choice([1, 3, 7]))
+        X = syn.normal_bf16(8000 + case, 4, (B * (k + 1), H), 1.0)
+        d = rng.integers(0, q_rows, size=(B, k)).astype(np.int32)
+        acc, nid, ml = vh.spec_verify_greedy_nvfp4_packed(to_torch_bf16(X), P, g, to_torch(d), B, k, q_rows)
+        torch.cuda.synchronize()
+        _, o_nid, o_ml, o_sec = orc.verify_greedy_nvfp4(X, q, s, g, None, B, k)
+        check_ids(nid.cpu().numpy(), ml.cpu().numpy(), o_nid, o_ml, o_sec,
+                  lambda r, v: float(orc.scores_nvfp4(X[r], q[v:v + 1], s[v:v + 1], g, nthreads=1)[0]), TOL_4BIT)
+        np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid.cpu().numpy(), d, B, k))
