@@ -205,7 +205,7 @@ __device__ __forceinline__ void block_argmax(const float4 (&s)[NT], int row0, in
 }
 
 // Work split: CTA c owns blocks [c*n/grid, (c+1)*n/grid); its (block, tile)
-// units are split evenly into 16 contiguous ranges, one per warp.  A block
+// units are split evenly into contiguous ranges, one per warp.  A block
 // cut by a range boundary is finished after all warps are done: each warp
 // leaves its partial sums of its first and last block in shared memory, and
 // the warp that holds the block's first tile adds the pieces in warp order.
