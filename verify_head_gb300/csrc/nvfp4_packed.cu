@@ -213,7 +213,7 @@ template <int NT, int kWarpsP>
 __global__ void __launch_bounds__(kWarpsP * 32, 1) k_nvfp4_packed(const Args a) {
     constexpr int kThreadsP = kWarpsP * 32;
     constexpr int N = 8 * NT;
-    constexpr int CH = NT == 1 ? 2 : 1;  // independent accumulation chains per n8 tile
+    constexpr int CH = 2;  // independent accumulation chains per n8 tile (even / odd MMAs)
     constexpr int D = NT == 1 ? kDepthNT1 : kDepthNT2;
     constexpr int kPrefetch = NT == 1 ? kPrefetchNT1 : kPrefetchNT2;
     extern __shared__ __align__(16) uint8_t xfrag[];  // [H/16 MMAs][NT][32 lanes][8 B]
