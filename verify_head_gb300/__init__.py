@@ -170,14 +170,24 @@ def _torch():
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the declared c_void_p argument types convert it
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = None  # torch's raw current-stream query, when this torch build has one
 
 
 def _stream_ptr(stream):
+    """cudaStream_t of `stream`, or of torch's current stream on the current device."""
+    global _raw_stream
     torch = _torch()
     if stream is None:
+        if _raw_stream is None:
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _require_cuda(*ts):
