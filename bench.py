@@ -143,7 +143,8 @@ class ClockSampler:
         """Median SM clock, the maximum, and every throttle reason seen over
         the whole run (warm-up, timed chains and the other workloads); the
         headline's timed region is also given on its own when it holds
-        samples (the driver's short runs time about 3 ms)."""
+        samples (a run of 20 steps times about 3 ms, less than one
+        sampling interval of some tools)."""
         if self.proc is None:
             return None
         try:

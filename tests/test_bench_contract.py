@@ -36,7 +36,7 @@ def test_command_line_offers_configs_and_oracle_threads():
 
 
 def test_reference_arm_under_torchrun_prints_once():
-    """Launched as the driver launches N > 1 (torchrun, 127.0.0.1): rank 0
+    """Launched as a multi-GPU run is launched (torchrun, 127.0.0.1): rank 0
     alone times the oracle and prints the line; the other rank exits 0."""
     import socket
     with socket.socket() as s:
