@@ -542,10 +542,17 @@ def measure_tiny(torch, vh, synth, timer):
     d = verify.draft_ids_from(o_nid)
     acc, nid, _ = vh.spec_verify_greedy(t_bf16(verify.X), t_bf16(W_full), torch.from_numpy(d).to(dev), 1, 3)
     o_acc = oracle.accept_len(o_nid[:3], d[0])
+    # timed as a decode loop calls it: workspace and outputs allocated once, outside the timed calls
     x0 = t_bf16(draft.hidden[0])
-    us_d = timer.time_calls(lambda: vh.mtp_draft_head_argmax(x0, W, cand), 20)
+    ws_d, ids_d = vh.workspace(1), torch.empty(1, dtype=torch.int32, device=dev)
+    ml_d = torch.empty(1, dtype=torch.float32, device=dev)
+    us_d = timer.time_calls(lambda: vh.mtp_draft_head_argmax(x0, W, cand, ids=ids_d, maxlogit=ml_d, ws=ws_d), 20)
     Xv, Wv, dv = t_bf16(verify.X), t_bf16(W_full), torch.from_numpy(d).to(dev)
-    us_v = timer.time_calls(lambda: vh.spec_verify_greedy(Xv, Wv, dv, 1, 3), 20)
+    ws_v = vh.workspace(4)
+    acc_v, nid_v = torch.empty(1, dtype=torch.int32, device=dev), torch.empty(4, dtype=torch.int32, device=dev)
+    ml_v = torch.empty(4, dtype=torch.float32, device=dev)
+    us_v = timer.time_calls(lambda: vh.spec_verify_greedy(Xv, Wv, dv, 1, 3, accept_len=acc_v, next_ids=nid_v,
+                                                          row_maxlogit=ml_v, ws=ws_v), 20)
     return {"workload": "4,096 x 256 head, 1,024 candidates, B=1 x 3 draft steps; verify 1 x 4 rows (seed 1)",
             "draft_ids_equal_oracle": f"{ids_ok}/3",
             "verify_next_ids_equal_oracle": f"{int((nid.cpu().numpy() == o_nid).sum())}/4",
