@@ -488,8 +488,15 @@ def summarize(line):
         s["verify_256x248320"] = {"rounds_per_s": v.get("rounds_per_s"), "us": v.get("median_us"),
                                   "hbm_frac": v.get("hbm_frac"), "tensor_frac_burst": v.get("tensor_frac_burst"),
                                   "tensor_frac_sustained": v.get("tensor_frac_sustained")}
+    if line.get("verify_rows") and "4" in line["verify_rows"]:
+        s["verify_batch1_4x248320"] = pair(line["verify_rows"]["4"])
+    r = line.get("mtp3_round")
+    if r:
+        s["mtp3_round_b1"] = {k: [v.get("mean_us"), v.get("rounds_per_s")] for k, v in r.items() if isinstance(v, dict)}
     if line.get("gather"):
         s["gather"] = pair(line["gather"], "mean_us")
+    if line.get("draft_batch"):
+        s["draft_batch_65536x2048"] = {k: pair(v, "mean_us") for k, v in line["draft_batch"].items()}
     nv = line.get("nvfp4")
     if nv:
         s["nvfp4_65536x4096"] = {**{k: pair(v, "mean_us") for k, v in nv.items() if k.startswith("B")},
@@ -512,6 +519,10 @@ def measure_extra(torch, vh, synth, timer, peaks, load_verify_golden, only="all"
         out["sweep"] = measure_sweep(torch, vh, synth, timer, peaks)
     if only in ("all", "gather"):
         out["gather"] = measure_gather(torch, vh, synth, timer, peaks)
+    if only in ("all", "draft_batch"):
+        out["draft_batch"] = measure_draft_batch(torch, vh, synth, timer, peaks)
+    if only in ("all", "mtp3_round"):
+        out["mtp3_round"] = measure_mtp3_round(torch, vh, synth, timer, peaks)
     if only in ("all", "chain"):
         out["chain_graph"] = measure_chain_graph(torch, vh, synth, timer, peaks)
     if only in ("all", "verify_nvfp4"):
@@ -648,6 +659,76 @@ def measure_sweep(torch, vh, synth, timer, peaks):
                           "hbm_frac": round(nbytes / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
         del Wc
     return sweep
+
+
+def measure_draft_batch(torch, vh, synth, timer, peaks):
+    """The bf16 draft head 65,536 x 2048 for 2 / 4 / 8 hidden rows per call
+    (warp-level MMAs fed from the weight stream): three draft steps per chain
+    as in the bench step, per call = chain / 3."""
+    dev = torch.device("cuda")
+    c = synth.draft_case(Vc=65_536, H=2048, B=8, steps=3, seed=2)
+    Wc = torch.from_numpy(c.W.view(np.int16)).to(dev).view(torch.bfloat16)
+    cc = torch.from_numpy(c.cand_ids).to(dev)
+    out = {}
+    for B in (2, 4, 8):
+        xs = [torch.from_numpy(np.ascontiguousarray(h[:B]).view(np.int16)).to(dev).view(torch.bfloat16)
+              for h in c.hidden]
+        wsb = vh.workspace(B)
+        ids = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(3)]
+        mls = [torch.empty(B, dtype=torch.float32, device=dev) for _ in range(3)]
+
+        def chain():
+            for k in range(3):
+                vh.mtp_draft_head_argmax(xs[k], Wc, cc, ids=ids[k], maxlogit=mls[k], ws=wsb)
+
+        us = [t / 3 for t in timer.time_calls(chain, 20)]
+        mean = statistics.mean(us)
+        nbytes = 65_536 * 2048 * 2 + 65_536 * 4 + B * 2048 * 2
+        out[f"B{B}"] = {"timing": "3-call chains, per call", "steps_per_s": round(1e6 / mean, 1), **stats(us),
+                        "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                        "kernel": "k_gemv_mma_bf16 (warp MMAs fed from the weight stream)"}
+    del Wc
+    return out
+
+
+def measure_mtp3_round(torch, vh, synth, timer, peaks):
+    """One batch-1 MTP3 decode round as the pages run it: three draft steps on
+    the 65,536 x 2048 candidate table (B = 1), each writing its id into the
+    draft-id buffer, then the greedy verify of the 4 rows against the full
+    248,320 x 2048 head, which reads those ids.  AUTO kernels (the tcgen05
+    verify) against the same round with the warp-MMA verify."""
+    dev = torch.device("cuda")
+    c = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
+    Wc = torch.from_numpy(c.W.view(np.int16)).to(dev).view(torch.bfloat16)
+    cc = torch.from_numpy(c.cand_ids).to(dev)
+    xs = [torch.from_numpy(np.ascontiguousarray(h).view(np.int16)).to(dev).view(torch.bfloat16) for h in c.hidden]
+    Wf = torch.from_numpy(synth.full_head(2, synth.V_FULL, 2048).view(np.int16)).to(dev).view(torch.bfloat16)
+    X = torch.from_numpy(synth.normal_bf16(4, synth.STREAM_VHIDDEN, (4, 2048), 1.0).view(np.int16)).to(dev)
+    X = X.view(torch.bfloat16)
+    draft = torch.zeros(1, 3, dtype=torch.int32, device=dev)
+    mld = [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(3)]
+    wsd, wsv = vh.workspace(1), vh.workspace(4)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    nid = torch.empty(4, dtype=torch.int32, device=dev)
+    mlv = torch.empty(4, dtype=torch.float32, device=dev)
+    out = {}
+    for name, path in (("auto", vh.VH_PATH_AUTO), ("warp_mma_verify", vh.VH_PATH_WARP_MMA)):
+        def rnd(path=path):
+            for k in range(3):
+                vh.mtp_draft_head_argmax(xs[k], Wc, cc, ids=draft[0, k:k + 1], maxlogit=mld[k], ws=wsd)
+            vh.spec_verify_greedy(X, Wf, draft, 1, 3, accept_len=acc, next_ids=nid, row_maxlogit=mlv, ws=wsv,
+                                  path=path)
+
+        us = timer.time_calls(rnd, 20)
+        mean = statistics.mean(us)
+        nbytes = 3 * (65_536 * 2048 * 2 + 65_536 * 4) + synth.V_FULL * 2048 * 2
+        out[name] = {"rounds_per_s": round(1e6 / mean, 1), **stats(us),
+                     "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "kernels": "3 x k_gemv_bf16<1> + " + ("k_verify_tc" if name == "auto" else "k_gemv_mma_bf16")}
+    out["workload"] = ("B = 1, k = 3: 3 draft calls on 65,536 x 2048 (one id each into the draft buffer) + verify "
+                       "of 4 rows against 248,320 x 2048; one round between one pair of CUDA events, L2 flushed")
+    del Wc, Wf
+    return out
 
 
 def measure_gather(torch, vh, synth, timer, peaks):
@@ -921,7 +1002,8 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="omit the verify / sweep / 4-bit measurements")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "tiny", "draft", "verify", "sweep", "nvfp4", "gather", "chain", "verify_nvfp4"],
+                    choices=["all", "tiny", "draft", "verify", "sweep", "nvfp4", "gather", "chain", "verify_nvfp4",
+                             "draft_batch", "mtp3_round"],
                     help="all = the bench line; others run one measurement only (for profiling)")
     ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5],
                     help="one workload by number: 1 tiny oracle check, 2 draft head 65,536 x 2048, "

@@ -87,7 +87,8 @@ VH_API size_t vh_workspace_bytes(int rows);
  *  cand_ids  device, int32 [Vc], ascending and distinct (precondition, not
  *            checked; ties are broken by id either way), values in [0, 2^31)
  *  B         1 <= B <= 256 (processed in groups of 8 hidden rows; each group
- *            reads W_cand once)
+ *            reads W_cand once: one row on the streaming GEMV, 2-8 rows on
+ *            warp-level MMAs when H % 256 == 0)
  *  H         16 <= H <= 65536, H % 16 == 0
  *  Vc        1 <= Vc <= 2^31 - 1
  *  ids       device, int32 [B] (out)
@@ -290,9 +291,11 @@ VH_API vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq,
 
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
-    VH_PATH_AUTO = 0,      /* tensor cores when H % 64 == 0, else CUDA cores */
+    VH_PATH_AUTO = 0,      /* tcgen05 when H % 64 == 0, else CUDA cores */
     VH_PATH_CUDA_CORE = 1, /* streaming GEMV, groups of 8 rows */
-    VH_PATH_TENSOR = 2     /* tcgen05 skinny GEMM, groups of 256 rows; VH_ERR_SHAPE if H % 64 != 0 */
+    VH_PATH_TENSOR = 2,    /* tcgen05 skinny GEMM, groups of 256 rows; VH_ERR_SHAPE if H % 64 != 0 */
+    VH_PATH_WARP_MMA = 3   /* warp-level MMAs fed from the weight stream, groups of 8 rows; VH_ERR_SHAPE
+                              unless H % 256 == 0 and H <= 10240 */
 } vh_path;
 
 /* spec_verify_greedy with an explicit kernel choice (same results up to fp32

@@ -198,16 +198,24 @@ def test_gather_fixed_plus_dynamic_full_head(vh, orc, syn):
 
 
 def test_gather_matches_candidate_table_kernel(vh, syn):
-    """Same candidate set as a sorted copied table: same ids and maxima."""
+    """Same candidate set as a sorted copied table: same ids and maxima.  One
+    hidden row runs the same streaming GEMV on both sides (bit-identical
+    maxima); four rows run the table on warp-level MMAs, which sum in another
+    fp32 order (ids identical, maxima within 1e-4)."""
     V, H = 30_000, 1024
     W = syn.normal_bf16(5, 1, (V, H), 0.02)
     cand = syn.sorted_subset(5, 2, V, 6000)
     x = syn.normal_bf16(6, 3, (4, H), 1.0)
     perm = np.random.default_rng(0).permutation(cand).astype(np.int32)
-    g_ids, g_ml = run_gather(vh, x, W, perm)
-    t_ids, t_ml = run_draft(vh, x, np.ascontiguousarray(W[cand]), cand)
+    table = np.ascontiguousarray(W[cand])
+    g_ids, g_ml = run_gather(vh, x[:1], W, perm)
+    t_ids, t_ml = run_draft(vh, x[:1], table, cand)
     np.testing.assert_array_equal(g_ids, t_ids)
     np.testing.assert_array_equal(g_ml, t_ml)
+    g_ids, g_ml = run_gather(vh, x, W, perm)
+    t_ids, t_ml = run_draft(vh, x, table, cand)
+    np.testing.assert_array_equal(g_ids, t_ids)
+    np.testing.assert_allclose(g_ml, t_ml, rtol=0, atol=1e-4)
 
 
 # ----------------------------------------------------------------------------

@@ -29,6 +29,7 @@ VH_ERR_DEVICE = -6
 VH_PATH_AUTO = 0
 VH_PATH_CUDA_CORE = 1
 VH_PATH_TENSOR = 2
+VH_PATH_WARP_MMA = 3
 
 # Every symbol the header declares (checked by the ABI tests).
 EXPORTS = (
@@ -277,7 +278,8 @@ def mtp_draft_head_argmax_nvfp4(hidden, Wq, scales, tensor_scale, cand_ids, ids=
 def spec_verify_greedy(hidden, W_full, draft_ids, B: int, k: int, accept_len=None, next_ids=None, row_maxlogit=None,
                        ws=None, stream=None, path: int = VH_PATH_AUTO, want_maxlogit: bool = True):
     """hidden [B*(k+1),H] bf16, W_full [V,H] bf16, draft_ids [B,k] int32
-    -> (accept_len [B], next_ids [B*(k+1)], row_maxlogit [B*(k+1)] or None)."""
+    -> (accept_len [B], next_ids [B*(k+1)], row_maxlogit [B*(k+1)] or None).
+    `path`: VH_PATH_AUTO / VH_PATH_CUDA_CORE / VH_PATH_TENSOR / VH_PATH_WARP_MMA."""
     torch = _torch()
     _require_cuda(hidden, W_full, draft_ids)
     R, H = hidden.shape

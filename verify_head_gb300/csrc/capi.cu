@@ -15,6 +15,7 @@ using vh::gemv_group;
 using vh::kMaxDraftB;
 using vh::kMaxH;
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
+constexpr int kMmaRows = 8;    // hidden rows per warp-MMA launch
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
@@ -97,8 +98,8 @@ vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const in
     const int grp = gemv_group(H);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
-        cudaError_t e = vh::launch_gemv_bf16(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
-                                             cand_ids, Vc, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s);
+        cudaError_t e = vh::launch_draft_group(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
+                                               cand_ids, Vc, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s);
         if (e != cudaSuccess) return launch_status(e);
     }
     return VH_OK;
@@ -183,8 +184,10 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     if (!hidden || !W_full || !draft_ids || !accept_len || !next_ids || !ws) return VH_ERR_NULL;
     if (B < 1 || k < 1 || k > 15 || H < 16 || H > kMaxH || H % 16 != 0 || V < 1) return VH_ERR_SHAPE;
     if ((long long)B * (k + 1) > 65536) return VH_ERR_SHAPE;
-    if (path != VH_PATH_AUTO && path != VH_PATH_CUDA_CORE && path != VH_PATH_TENSOR) return VH_ERR_SHAPE;
+    if (path != VH_PATH_AUTO && path != VH_PATH_CUDA_CORE && path != VH_PATH_TENSOR && path != VH_PATH_WARP_MMA)
+        return VH_ERR_SHAPE;
     if (path == VH_PATH_TENSOR && H % 64 != 0) return VH_ERR_SHAPE;
+    if (path == VH_PATH_WARP_MMA && !vh::gemv_mma_supported(1, H)) return VH_ERR_SHAPE;
     if (!aligned(hidden, 16) || !aligned(W_full, 32) || !aligned(draft_ids, 4) || !aligned(accept_len, 4) ||
         !aligned(next_ids, 4) || !aligned(row_maxlogit, 4) || !aligned(ws, 16))
         return VH_ERR_ALIGN;
@@ -199,9 +202,13 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
 
     // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
     // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
-    // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.
-    bool tensor = (path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0);
-    const int group = tensor ? kTcRows : gemv_group(H);
+    // on the 248,320 x 2048 head), so AUTO takes the tcgen05 kernels whenever the width allows.  The
+    // warp-level MMAs fed from the weight stream (VH_PATH_WARP_MMA) beat them only when verify calls
+    // follow each other (4 rows: 165 against 167 us per call); a single call (172-176 against 170 us)
+    // and a batch-1 round after three draft calls (306 against 300 us) favour tcgen05.
+    const bool wmma = path == VH_PATH_WARP_MMA;
+    const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
+    const int group = wmma ? kMmaRows : tensor ? kTcRows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += group) {
         const int nr = std::min(group, R - r0);
         vh::AcceptTail tail;
@@ -214,7 +221,9 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
         }
         float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
         cudaError_t e;
-        if (tensor) {
+        if (wmma) {
+            e = vh::launch_gemv_mma_bf16(X + (size_t)r0 * H, nr, H, W, nullptr, V, w, next_ids + r0, ml, tail, s);
+        } else if (tensor) {
             e = vh::launch_verify_tc(X + (size_t)r0 * H, nr, H, W, V, w, next_ids + r0, ml, tail, s);
         } else {
             e = vh::launch_gemv_bf16(X + (size_t)r0 * H, nr, H, W, nullptr, V, w, next_ids + r0, ml, tail, s);

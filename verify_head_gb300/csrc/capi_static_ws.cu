@@ -90,12 +90,12 @@ vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand
         return VH_ERR_LAUNCH;
     }
     const vh::Workspace w = vh::ws_view(scratch);
-    const int grp = vh::gemv_group(H);  // the same launch groups as mtp_draft_head_argmax
+    const int grp = vh::gemv_group(H);  // the same launch groups and kernels as mtp_draft_head_argmax
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
-        cudaError_t e = vh::launch_gemv_bf16(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
-                                             cand_ids, Vc, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s);
+        cudaError_t e = vh::launch_draft_group(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
+                                               cand_ids, Vc, w, ids + b0, maxlogit + b0, vh::AcceptTail{}, s);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return VH_ERR_LAUNCH;

@@ -1,0 +1,329 @@
+// bf16 head scored for 1-8 hidden rows on warp-level tensor-core MMAs fed
+// straight from the weight stream, fused with the argmax, the candidate-id
+// mapping and (for verify) the acceptance scan.  Serves the draft head
+// ("少读一张大表，草稿路径才真正快起来": a candidate table, the winning
+// candidate's global id) for small batches and the batch-1 MTP verify rows
+// (the target scores k+1 rows against the full head).
+//
+// MMA roles.  mma.m16n8k16 with A = the hidden rows (M = 16: up to 8 real
+// rows, the upper 8 are zero), B = 8 head rows (N = 8), fp32 accumulation.
+// Lane L (g = L/4, t = L%4) supplies B for head row g of the group, so a warp
+// streams 8 head rows at once, 512 contiguous bytes of each per step: load i
+// (i = 0..3) of lane t reads the row's bytes 128i + 32t .. +31, so the four
+// lanes of a row read one whole 128-byte line per instruction.
+//
+// K order.  Within a 256-element step, MMA j = 4i + m (i, m = 0..3) gives lane
+// (g, t) the physical elements 64i + 16t + 4m + {0,1} for its K slots {2t,
+// 2t+1} and 64i + 16t + 4m + {2,3} for {2t+8, 2t+9}, on A and B alike: each
+// MMA sums the same products as the plain order, and a lane's B registers for
+// MMA j are registers 2m and 2m+1 of its load i.  The hidden rows sit in
+// shared memory in that fragment order: lane L's 8 bytes for (step s, MMA j)
+// are row g's elements 256s + 64i + 16t + 4m .. +3, and a warp reads 256
+// consecutive bytes per MMA.
+//
+// Output.  Accumulator registers c0 / c1 of lane (g, t) are hidden row g's
+// scores of head rows 2t and 2t+1 of the group; c2 / c3 belong to the zero
+// rows.  Each lane keeps one packed (score, id) key for its hidden row; the
+// four lanes of a row, the warps of a CTA and the CTAs merge by max, and the
+// last CTA (ticket counter) writes ids / max logits, runs the optional
+// acceptance scan and re-zeroes the workspace.
+//
+// Work split.  Each CTA owns whole 8-row groups; inside a CTA the (group,
+// 256-element step) units are split evenly over the warps, and a group cut
+// between two warps is summed in shared memory in warp order.
+#include <algorithm>
+#include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "vh_kernels.h"
+#include "vh_ptx.cuh"
+
+namespace vh {
+namespace gmma {
+
+constexpr int kWarpsG = 8;
+constexpr int kThreadsG = kWarpsG * 32;
+constexpr int kStepK = 256;   // elements of K per step (512 bytes of each head row)
+constexpr int kRowsG = 8;     // head rows per warp group (MMA N)
+constexpr int kMaxRows = 8;   // hidden rows per launch
+
+struct Args {
+    const uint16_t* x;  // bf16 [nb][H]
+    const uint16_t* W;  // bf16 [n_rows][H]
+    const int32_t* cand;
+    int nb, H, n_rows, n_groups;
+    Workspace ws;
+    unsigned int* err;
+    int32_t* ids;
+    float* maxlogit;
+    AcceptTail tail;
+};
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+// D += A (16 x 16 bf16, rows g / g+8) * B (16 x 8 bf16), fp32 accumulate; the
+// rows g+8 of A are zero.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+struct Seg {  // this lane's 128 bytes of one head row's step: elements 64i + 16t .. +15, i = 0..3
+    U32x8 v[4];
+};
+
+__device__ __forceinline__ void load_seg(Seg& s, const uint16_t* p) {  // p: the step's element 16t of the row
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s.v[i] = ld_stream32(p + i * 64);
+}
+
+// The 16 MMAs of one step: B from the lane's registers, A from shared memory.
+__device__ __forceinline__ void step_mma(const Seg& w, uint32_t afrag, float (&c0)[4], float (&c1)[4]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint2 a = lds64(afrag + (uint32_t)(j * 256));
+        const uint32_t b0 = w.v[j >> 2].v[2 * (j & 3)], b1 = w.v[j >> 2].v[2 * (j & 3) + 1];
+        if (j & 1)
+            mma_bf16_16816(c1, a.x, a.y, b0, b1);
+        else
+            mma_bf16_16816(c0, a.x, a.y, b0, b1);
+    }
+}
+
+__global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
+    extern __shared__ __align__(16) uint8_t xfrag[];  // [H/256 steps][16 MMAs][32 lanes][8 B]
+    __shared__ float2 cut[kWarpsG][2][32];             // partial scores of groups cut between warps
+    __shared__ unsigned long long merge[kMaxRows];
+    __shared__ unsigned int s_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = a.H, n_steps = H / kStepK;
+
+    // CTA c owns the 8-row groups [G0, G1); its (group, step) units are split
+    // evenly into contiguous ranges, one per warp.  A group cut by a range
+    // boundary is finished after all warps are done: each warp leaves its
+    // partial scores of its first and last group in shared memory and the
+    // warp that holds the group's first step adds the pieces in warp order.
+    const int G0 = (int)((long long)blockIdx.x * a.n_groups / gridDim.x);
+    const int G1 = (int)((long long)(blockIdx.x + 1) * a.n_groups / gridDim.x);
+    const int CU = (G1 - G0) * n_steps;
+    auto u_begin = [&](int w) { return (int)((long long)w * CU / kWarpsG); };
+    const int v_lo = u_begin(warp), v_hi = u_begin(warp + 1);
+
+    auto unit_ptr = [&](int v) -> const uint16_t* {  // this lane's 64 elements of unit v
+        const int r = (G0 + v / n_steps) * kRowsG + g;
+        return a.W + (size_t)(r < a.n_rows ? r : 0) * H + (size_t)(v % n_steps) * kStepK + (size_t)t * 16;
+    };
+    // the 128-byte lines of a group's eight rows head for L2 (lane L: row L/4, lines L%4, L%4 + 4, ...).
+    // Done once, for the warp's first group, while the kernel waits for the previous one; prefetching
+    // the next group from inside the loop competed with the demand loads (0.74 against 0.91 of HBM on
+    // the 248,320-row head).
+    auto prefetch_group = [&](int grp) {
+        const int r = (G0 + grp) * kRowsG + g;
+        if (r < a.n_rows)
+            for (int c = t * 64; c < H; c += 256) prefetch_l2(a.W + (size_t)r * H + c);
+    };
+    // keys of one finished group (this lane: hidden row g, head rows 2t and 2t+1)
+    unsigned long long best = 0ull;
+    auto finish_group = [&](int grp, float s0, float s1) {
+        if (g >= a.nb) return;
+        const int r0 = (G0 + grp) * kRowsG + 2 * t;
+        const float sc[2] = {s0, s1};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = r0 + h;
+            if (r < a.n_rows) {
+                const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
+                const unsigned long long k = make_key(sc[h], gid);
+                best = k > best ? k : best;
+            }
+        }
+    };
+
+    pdl_launch_dependents();
+    if (v_lo < v_hi) prefetch_group(v_lo / n_steps);  // the head never changes: before the dependency wait
+    if (threadIdx.x < kMaxRows) merge[threadIdx.x] = 0ull;
+    pdl_wait();  // the hidden rows and the workspace may come from the previous kernel
+
+    // hidden rows -> fragment order (rows >= nb are zero)
+    for (int e = threadIdx.x; e < n_steps * 16 * 32; e += blockDim.x) {
+        const int L = e & 31, j = (e >> 5) & 15, st = e >> 9;
+        const int gg = L >> 2, tt = L & 3;
+        uint2 v = make_uint2(0u, 0u);
+        if (gg < a.nb)
+            v = *reinterpret_cast<const uint2*>(a.x + (size_t)gg * H + st * kStepK + (j >> 2) * 64 + tt * 16 +
+                                                (j & 3) * 4);
+        reinterpret_cast<uint2*>(xfrag)[e] = v;
+    }
+    __syncthreads();
+
+    const uint32_t afrag0 = ptx::smem_u32(xfrag) + (uint32_t)lane * 8u;
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    bool first = true;
+    const bool starts_cut = v_lo % n_steps != 0;
+    Seg w[2];
+    if (v_lo < v_hi) load_seg(w[0], unit_ptr(v_lo));
+    for (int v0 = v_lo; v0 < v_hi; v0 += 2) {
+#pragma unroll
+        for (int d = 0; d < 2; ++d) {
+            const int v = v0 + d;
+            if (v < v_hi) {
+                if (v + 1 < v_hi) load_seg(w[d ^ 1], unit_ptr(v + 1));
+                const int grp = v / n_steps, st = v % n_steps;
+                step_mma(w[d], afrag0 + (uint32_t)(st * 16 * 256), c0, c1);
+                const bool grp_end = st + 1 == n_steps, range_end = v + 1 == v_hi;
+                if (grp_end || range_end) {
+                    const float s0 = c0[0] + c1[0], s1 = c0[1] + c1[1];
+                    if (!(first && starts_cut) && grp_end)
+                        finish_group(grp, s0, s1);
+                    else  // a piece of a cut group: slot 0 = this warp's first group, 1 = its last
+                        cut[warp][first ? 0 : 1][lane] = make_float2(s0, s1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c0[i] = c1[i] = 0.f;
+                    first = false;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // finish the cut group that starts in this warp's range (its last group, cut at the range end)
+    if (v_lo < v_hi && v_hi % n_steps != 0) {
+        const int jg = (v_hi - 1) / n_steps;  // CTA-local group
+        if (jg * n_steps >= v_lo) {          // its first step is ours: add the pieces in warp order
+            float s0 = 0.f, s1 = 0.f;
+            for (int ww = warp; ww < kWarpsG; ++ww) {
+                const int wl = u_begin(ww), wh = u_begin(ww + 1);
+                if (wl >= (jg + 1) * n_steps) break;
+                if (wh <= wl) continue;  // a warp without units
+                const float2 p = cut[ww][(wl / n_steps == jg) ? 0 : 1][lane];
+                s0 += p.x;
+                s1 += p.y;
+            }
+            finish_group(jg, s0, s1);
+        }
+    }
+
+    // the four lanes of a hidden row, then the warps, then the CTAs
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, m);
+        best = o > best ? o : best;
+    }
+    if (t == 0 && g < a.nb && best != 0ull) atomicMax(&merge[g], best);
+    __syncthreads();
+    if (threadIdx.x < a.nb && merge[threadIdx.x] != 0ull) atomicMax(a.ws.keys + threadIdx.x, merge[threadIdx.x]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x < a.nb) {
+        const unsigned long long k = atomicExch(a.ws.keys + threadIdx.x, 0ull);
+        vh_guard(k != 0ull, a.err);  // every hidden row has a winner
+        a.ids[threadIdx.x] = (int32_t)key_gid(k);
+        if (a.maxlogit != nullptr) a.maxlogit[threadIdx.x] = key_score(k);
+    }
+    if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
+    if (a.tail.draft != nullptr) {
+        __threadfence();
+        __syncthreads();
+        const int k = a.tail.k;
+        for (int b = threadIdx.x; b < a.tail.B; b += blockDim.x) {
+            const volatile int32_t* nid = a.tail.next_ids + (size_t)b * (k + 1);
+            const int32_t* d = a.tail.draft + (size_t)b * k;
+            int acc = 0;
+            while (acc < k && nid[acc] == d[acc]) ++acc;
+            a.tail.accept_len[b] = acc;
+        }
+    }
+}
+
+}  // namespace gmma
+
+bool gemv_mma_supported(int nb, int H) {  // 1-8 hidden rows, H % 256 == 0, hidden rows fit shared memory
+    return nb >= 1 && nb <= gmma::kMaxRows && H >= gmma::kStepK && H % gmma::kStepK == 0 &&
+           (size_t)H * 16 <= 160 * 1024;
+}
+
+cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    using namespace gmma;
+    if (!gemv_mma_supported(nb, H) || n_rows < 1 || n_rows > INT_MAX - kRowsG) return cudaErrorNotSupported;
+    Args a{};
+    a.x = x;
+    a.W = W;
+    a.cand = cand;
+    a.nb = nb;
+    a.H = H;
+    a.n_rows = n_rows;
+    a.n_groups = (n_rows + kRowsG - 1) / kRowsG;
+    a.ws = ws;
+    a.err = ws.ticket + 1;
+    a.ids = ids;
+    a.maxlogit = maxlogit;
+    a.tail = tail;
+    const size_t smem = (size_t)H * 16;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemv_mma_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    static std::mutex mu;
+    static std::map<std::tuple<size_t, int>, int> cache;  // (shared memory, device) -> resident CTAs per SM
+    int dev = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto key = std::make_tuple(smem, dev);
+        const auto it = cache.find(key);
+        if (it != cache.end()) {
+            per_sm = it->second;
+        } else {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_mma_bf16, kThreadsG, smem);
+            if (e != cudaSuccess) return e;
+            cache[key] = per_sm;
+        }
+    }
+    if (per_sm < 1) return cudaErrorNotSupported;
+    // one resident wave, at least one 8-row group per CTA
+    const long long grid = std::max(1LL, std::min((long long)sm_count() * per_sm, (long long)a.n_groups));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreadsG);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gemv_mma_bf16, a);
+}
+
+}  // namespace vh
+
+namespace vh {
+
+cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                               Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    // one hidden row: the CUDA-core GEMV (0.88 of HBM on 65,536 x 2048 against 0.84 for the warp MMAs);
+    // 2-8 rows: the warp MMAs (0.83), where the GEMV slows with every row it holds
+    if (nb >= 2 && gemv_mma_supported(nb, H))
+        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
+    return launch_gemv_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
+}
+
+}  // namespace vh

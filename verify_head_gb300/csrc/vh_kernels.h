@@ -39,6 +39,18 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
                              Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
                              int gather_V = 0);
 
+// bf16 head for 1-8 hidden rows on warp-level MMAs fed straight from the
+// weight stream (mma.m16n8k16, hidden rows as A, 8 head rows as B) + argmax.
+// gemv_mma_supported: H % 256 == 0 and the hidden rows (16*H bytes in
+// fragment order) fit shared memory.  Returns cudaErrorNotSupported otherwise.
+bool gemv_mma_supported(int nb, int H);
+cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+// One launch group (nb <= gemv_group(H) hidden rows) of the bf16 draft head:
+// the kernel both draft entry points use for that group size.
+cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                               Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+
 // Block-scaled 4-bit (E2M1 codes, E4M3 block scales, fp32 tensor scale)
 // GEMV + argmax on CUDA cores, nb <= 8.
 cudaError_t launch_gemv_nvfp4(const uint16_t* x, int nb, int H, const uint8_t* Wq, const uint8_t* scales, float g,
