@@ -1,7 +1,7 @@
 """Seeded random shapes through every entry point against the oracle: batch
 sizes, widths (every allowed multiple), table sizes, k and gathered id lists
 drawn at random, so that kernel selection boundaries, ragged tails and group
-splits are hit in combinations no hand-picked list covers (54 cases by
+splits are hit in combinations no hand-picked list covers (62 cases by
 default; VH_FUZZ_SCALE multiplies every family)."""
 import os
 
@@ -120,6 +120,42 @@ def test_fuzz_verify_bf16(vh, orc, syn, case):
     nid = nid.cpu().numpy()
     check_ids(nid, ml.cpu().numpy(), o_nid, o_ml, o_sec, lambda r, v: orc.dot_bf16(X[r], W[v]), TOL_BF16)
     np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid, draft, B, k))
+
+
+@pytest.mark.parametrize("case", range(8 * SCALE))
+def test_fuzz_warp_mma_bf16(vh, orc, syn, case):
+    """The bf16 head on warp-level MMAs: the draft at 2-8 rows (its default
+    for widths that are multiples of 256) and the verify on VH_PATH_WARP_MMA
+    (one or several 8-row passes), at every width it takes up to 10,240."""
+    import torch
+    rng = np.random.default_rng(1400 + case)
+    H = 256 * int(rng.integers(1, 41))  # 256 .. 10,240
+    if case % 2 == 0:
+        B = int(rng.integers(2, 9))
+        Vc = _rows_for(rng, MAC_BUDGET, B * H)
+        W = syn.normal_bf16(10_000 + case, 1, (Vc, H), 0.02)
+        cand = syn.sorted_subset(10_000 + case, 2, 248_320, Vc)
+        x = syn.normal_bf16(11_000 + case, 3, (B, H), 1.0)
+        ids, ml = vh.mtp_draft_head_argmax(to_torch_bf16(x), to_torch_bf16(W), to_torch(cand))
+        torch.cuda.synchronize()
+        o_ids, o_ml, o_sec = orc.draft_argmax(x, W, cand)
+        check_ids(ids.cpu().numpy(), ml.cpu().numpy(), o_ids, o_ml, o_sec,
+                  lambda r, g: orc.dot_bf16(x[r], W[int(np.searchsorted(cand, g))]), TOL_BF16)
+    else:
+        k = int(rng.integers(1, 8))
+        B = int(rng.integers(1, max(2, 24 // (k + 1))))
+        R = B * (k + 1)
+        V = _rows_for(rng, MAC_BUDGET, R * H, hi=30_000)
+        W = syn.normal_bf16(12_000 + case, 1, (V, H), 0.02)
+        X = syn.normal_bf16(13_000 + case, 4, (R, H), 1.0)
+        draft = rng.integers(0, V, size=(B, k)).astype(np.int32)
+        acc, nid, ml = vh.spec_verify_greedy(to_torch_bf16(X), to_torch_bf16(W), to_torch(draft), B, k,
+                                             path=vh.VH_PATH_WARP_MMA)
+        torch.cuda.synchronize()
+        _, o_nid, o_ml, o_sec = orc.verify_greedy(X, W, None, B, k)
+        nid = nid.cpu().numpy()
+        check_ids(nid, ml.cpu().numpy(), o_nid, o_ml, o_sec, lambda r, v: orc.dot_bf16(X[r], W[v]), TOL_BF16)
+        np.testing.assert_array_equal(acc.cpu().numpy(), accept_scan(nid, draft, B, k))
 
 
 @pytest.mark.parametrize("case", range(6 * SCALE))
