@@ -1,6 +1,7 @@
 """The bf16 head on warp-level MMAs fed from the weight stream (k_gemv_mma_bf16):
-the draft head for 2-8 hidden rows (its default there) and greedy verify on
-VH_PATH_WARP_MMA, against the CPU oracle through the C ABI."""
+the draft head for 2-8 hidden rows (its default there) and greedy verify (on
+VH_PATH_WARP_MMA, and under AUTO for up to 8 rows against heads under 256
+MiB), against the CPU oracle through the C ABI."""
 import os
 
 import numpy as np
@@ -137,6 +138,14 @@ def test_verify_shapes(vh, orc, syn, B, k, V, H):
     W = syn.normal_bf16(V + H + 5, 1, (V, H), 0.02)
     X = syn.normal_bf16(B + k + 7, 4, (B * (k + 1), H), 1.0)
     check_verify(vh, orc, syn, X, W, B, k, path, seed=B * 100 + k + 1)
+
+
+# AUTO takes the warp MMAs for up to 8 rows against heads under 256 MiB (H % 256 == 0)
+@pytest.mark.parametrize("B,k,V,H", [(1, 3, 4096, 256), (2, 3, 20_000, 512), (1, 7, 3001, 2048)])
+def test_verify_auto_small_heads(vh, orc, syn, B, k, V, H):
+    W = syn.normal_bf16(V + H + 9, 1, (V, H), 0.02)
+    X = syn.normal_bf16(B + k + 13, 4, (B * (k + 1), H), 1.0)
+    check_verify(vh, orc, syn, X, W, B, k, vh.VH_PATH_AUTO, seed=B * 100 + k + 7)
 
 
 def test_warp_mma_path_refuses_other_widths(vh):

@@ -16,6 +16,7 @@ using vh::kMaxDraftB;
 using vh::kMaxH;
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
 constexpr int kMmaRows = 8;    // hidden rows per warp-MMA launch
+constexpr long long kMmaMaxHeadBytes = 256ll << 20;  // AUTO verify: warp MMAs below this head size
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
@@ -202,11 +203,14 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
 
     // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
     // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
-    // on the 248,320 x 2048 head), so AUTO takes the tcgen05 kernels whenever the width allows.  The
-    // warp-level MMAs fed from the weight stream (VH_PATH_WARP_MMA) beat them only when verify calls
-    // follow each other (4 rows: 165 against 167 us per call); a single call (172-176 against 170 us)
-    // and a batch-1 round after three draft calls (306 against 300 us) favour tcgen05.
-    const bool wmma = path == VH_PATH_WARP_MMA;
+    // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.  For up to
+    // 8 rows the warp-level MMAs fed from the weight stream start faster than the tcgen05 kernel (no
+    // TMEM, barrier or tensor-map set-up): on heads under 256 MiB a 4-row call took 0.75-0.98 of the
+    // tcgen05 time (4,096 x 256: 10.2 against 12.3 us), on larger heads 1.00-1.02 (248,320 x 2048: 173
+    // against 170 us; a draft + verify round 306 against 300 us), so AUTO switches at 256 MiB.
+    const bool wmma = (path == VH_PATH_WARP_MMA) ||
+                      (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H) &&
+                       (long long)V * H * 2 < kMmaMaxHeadBytes);
     const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
     const int group = wmma ? kMmaRows : tensor ? kTcRows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += group) {
