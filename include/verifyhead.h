@@ -87,8 +87,9 @@ VH_API size_t vh_workspace_bytes(int rows);
  *  cand_ids  device, int32 [Vc], ascending and distinct (precondition, not
  *            checked; ties are broken by id either way), values in [0, 2^31)
  *  B         1 <= B <= 256 (processed in groups of 8 hidden rows; each group
- *            reads W_cand once: one row on the streaming GEMV, 2-8 rows on
- *            warp-level MMAs when H % 256 == 0)
+ *            reads W_cand once: 2-8 rows on warp-level MMAs when H % 256 ==
+ *            0, one row on the streaming GEMV, or on the warp-level MMAs
+ *            for a table of 512 MiB or more)
  *  H         16 <= H <= 65536, H % 16 == 0
  *  Vc        1 <= Vc <= 2^31 - 1
  *  ids       device, int32 [B] (out)

@@ -55,6 +55,22 @@ vh_status launch_status(cudaError_t e) {
 
 }  // namespace
 
+namespace vh {
+
+cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                               Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    // 2-8 rows: the warp MMAs (0.81-0.82 of HBM on 65,536 x 2048), where the GEMV slows with every row it
+    // holds.  One row: the CUDA-core GEMV on tables under 512 MiB (it starts faster: 256 MiB 45.5 against
+    // 47.8 us, 384 MiB 69.7 against 70.0 us per chained call), the warp MMAs from 512 MiB up (88.2 against
+    // 89.8 us; the 248,320 x 2048 head 160.5-161.3 against 167.2 us, 0.93 against 0.90 of HBM)
+    constexpr long long kOneRowMmaBytes = 512ll << 20;
+    if (gemv_mma_supported(nb, H) && (nb >= 2 || (long long)n_rows * H * 2 >= kOneRowMmaBytes))
+        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
+    return launch_gemv_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
+}
+
+}  // namespace vh
+
 extern "C" {
 
 int vh_version(void) { return 10000; }

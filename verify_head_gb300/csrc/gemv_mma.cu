@@ -315,15 +315,3 @@ cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_
 
 }  // namespace vh
 
-namespace vh {
-
-cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
-                               Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
-    // one hidden row: the CUDA-core GEMV (0.88 of HBM on 65,536 x 2048 against 0.84 for the warp MMAs);
-    // 2-8 rows: the warp MMAs (0.83), where the GEMV slows with every row it holds
-    if (nb >= 2 && gemv_mma_supported(nb, H))
-        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
-    return launch_gemv_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
-}
-
-}  // namespace vh
