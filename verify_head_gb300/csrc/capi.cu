@@ -16,7 +16,6 @@ using vh::kMaxDraftB;
 using vh::kMaxH;
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
 constexpr int kMmaRows = 8;    // hidden rows per warp-MMA launch
-constexpr long long kMmaMaxHeadBytes = 256ll << 20;  // AUTO verify: warp MMAs below this head size
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
@@ -57,6 +56,15 @@ vh_status launch_status(cudaError_t e) {
 
 namespace vh {
 
+// Warp-MMA step length.  For 2-8 rows against heads of 768 MiB or more each warp streams 1 KiB of every
+// row per step: 4 rows on the 248,320 x 2048 head took 166.9-168.2 against 172.0-173.9 us with 512-byte
+// steps.  Below that, and for one row at every size, 512-byte steps are as fast or faster (4 rows on 768
+// MiB: 140.1 / 140.3 us; one row on the full head: 160.0 against 161.0 us per chained call).
+static bool long_steps(int nb, long long head_bytes) {
+    constexpr long long kLongStepBytes = 768ll << 20;
+    return nb >= 2 && head_bytes >= kLongStepBytes;
+}
+
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
     // 2-8 rows: the warp MMAs (0.81-0.82 of HBM on 65,536 x 2048), where the GEMV slows with every row it
@@ -64,8 +72,9 @@ cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t*
     // 47.8 us, 384 MiB 69.7 against 70.0 us per chained call), the warp MMAs from 512 MiB up (88.2 against
     // 89.8 us; the 248,320 x 2048 head 160.5-161.3 against 167.2 us, 0.93 against 0.90 of HBM)
     constexpr long long kOneRowMmaBytes = 512ll << 20;
-    if (gemv_mma_supported(nb, H) && (nb >= 2 || (long long)n_rows * H * 2 >= kOneRowMmaBytes))
-        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
+    const long long bytes = (long long)n_rows * H * 2;
+    if (gemv_mma_supported(nb, H) && (nb >= 2 || bytes >= kOneRowMmaBytes))
+        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s, long_steps(nb, bytes));
     return launch_gemv_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
 }
 
@@ -220,13 +229,13 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
     // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
     // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.  For up to
-    // 8 rows the warp-level MMAs fed from the weight stream start faster than the tcgen05 kernel (no
-    // TMEM, barrier or tensor-map set-up): on heads under 256 MiB a 4-row call took 0.75-0.98 of the
-    // tcgen05 time (4,096 x 256: 10.2 against 12.3 us), on larger heads 1.00-1.02 (248,320 x 2048: 173
-    // against 170 us; a draft + verify round 306 against 300 us), so AUTO switches at 256 MiB.
+    // 8 rows the warp-level MMAs fed from the weight stream go first (H % 256 == 0): they start faster
+    // than the tcgen05 kernel (no TMEM, barrier or tensor-map set-up).  A 4-row call took 0.92-0.98 of
+    // the tcgen05 time from 128 to 768 MiB (256 MiB: 54.5 against 59.4 us) and 0.99-1.00 on the
+    // 248,320 x 2048 head (166.9 against 167.3 us), and a batch-1 MTP3 round (three one-row drafts on
+    // 65,536 x 2048, then this verify) took 289.9 against 294.3 us.
     const bool wmma = (path == VH_PATH_WARP_MMA) ||
-                      (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H) &&
-                       (long long)V * H * 2 < kMmaMaxHeadBytes);
+                      (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H));
     const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
     const int group = wmma ? kMmaRows : tensor ? kTcRows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += group) {
@@ -242,7 +251,8 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
         float* ml = row_maxlogit ? row_maxlogit + r0 : nullptr;
         cudaError_t e;
         if (wmma) {
-            e = vh::launch_gemv_mma_bf16(X + (size_t)r0 * H, nr, H, W, nullptr, V, w, next_ids + r0, ml, tail, s);
+            e = vh::launch_gemv_mma_bf16(X + (size_t)r0 * H, nr, H, W, nullptr, V, w, next_ids + r0, ml, tail, s,
+                                         vh::long_steps(nr, (long long)V * H * 2));
         } else if (tensor) {
             e = vh::launch_verify_tc(X + (size_t)r0 * H, nr, H, W, V, w, next_ids + r0, ml, tail, s);
         } else {

@@ -45,7 +45,8 @@ namespace gmma {
 
 constexpr int kWarpsG = 8;
 constexpr int kThreadsG = kWarpsG * 32;
-constexpr int kStepK = 256;   // elements of K per step (512 bytes of each head row)
+constexpr int kStepK = 256;   // elements of K per step, short steps (512 bytes of each head row)
+constexpr int kStepLong = 512;  // long steps (1 KiB of each head row), single-buffered
 constexpr int kRowsG = 8;     // head rows per warp group (MMA N)
 constexpr int kMaxRows = 8;   // hidden rows per launch
 
@@ -81,19 +82,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
-struct Seg {  // this lane's 128 bytes of one head row's step: elements 64i + 16t .. +15, i = 0..3
-    U32x8 v[4];
+template <int STEP>
+struct Seg {  // this lane's part of one head row's step: elements 64i + 16t .. +15, i < STEP/64
+    U32x8 v[STEP / 64];
 };
 
-__device__ __forceinline__ void load_seg(Seg& s, const uint16_t* p) {  // p: the step's element 16t of the row
+template <int STEP>
+__device__ __forceinline__ void load_seg(Seg<STEP>& s, const uint16_t* p) {  // p: the step's element 16t of the row
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s.v[i] = ld_stream32(p + i * 64);
+    for (int i = 0; i < STEP / 64; ++i) s.v[i] = ld_stream32(p + i * 64);
 }
 
-// The 16 MMAs of one step: B from the lane's registers, A from shared memory.
-__device__ __forceinline__ void step_mma(const Seg& w, uint32_t afrag, float (&c0)[4], float (&c1)[4]) {
+// The STEP/16 MMAs of one step: B from the lane's registers, A from shared memory.
+template <int STEP>
+__device__ __forceinline__ void step_mma(const Seg<STEP>& w, uint32_t afrag, float (&c0)[4], float (&c1)[4]) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < STEP / 16; ++j) {
         const uint2 a = lds64(afrag + (uint32_t)(j * 256));
         const uint32_t b0 = w.v[j >> 2].v[2 * (j & 3)], b1 = w.v[j >> 2].v[2 * (j & 3) + 1];
         if (j & 1)
@@ -103,14 +107,17 @@ __device__ __forceinline__ void step_mma(const Seg& w, uint32_t afrag, float (&c
     }
 }
 
+// STEP: K elements per step (256 or 512); NBUF: steps in registers per warp (2 or 1).
+template <int STEP, int NBUF>
 __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
-    extern __shared__ __align__(16) uint8_t xfrag[];  // [H/256 steps][16 MMAs][32 lanes][8 B]
+    constexpr int kMmaStep = STEP / 16;                  // MMAs per step
+    extern __shared__ __align__(16) uint8_t xfrag[];  // [H/STEP steps][STEP/16 MMAs][32 lanes][8 B]
     __shared__ float2 cut[kWarpsG][2][32];             // partial scores of groups cut between warps
     __shared__ unsigned long long merge[kMaxRows];
     __shared__ unsigned int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int H = a.H, n_steps = H / kStepK;
+    const int H = a.H, n_steps = H / STEP;
 
     // CTA c owns the 8-row groups [G0, G1); its (group, step) units are split
     // evenly into contiguous ranges, one per warp.  A group cut by a range
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
 
     auto unit_ptr = [&](int v) -> const uint16_t* {  // this lane's 64 elements of unit v
         const int r = (G0 + v / n_steps) * kRowsG + g;
-        return a.W + (size_t)(r < a.n_rows ? r : 0) * H + (size_t)(v % n_steps) * kStepK + (size_t)t * 16;
+        return a.W + (size_t)(r < a.n_rows ? r : 0) * H + (size_t)(v % n_steps) * STEP + (size_t)t * 16;
     };
     // the 128-byte lines of a group's eight rows head for L2 (lane L: row L/4, lines L%4, L%4 + 4, ...).
     // Done once, for the warp's first group, while the kernel waits for the previous one; prefetching
@@ -159,12 +166,12 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     pdl_wait();  // the hidden rows and the workspace may come from the previous kernel
 
     // hidden rows -> fragment order (rows >= nb are zero)
-    for (int e = threadIdx.x; e < n_steps * 16 * 32; e += blockDim.x) {
-        const int L = e & 31, j = (e >> 5) & 15, st = e >> 9;
+    for (int e = threadIdx.x; e < n_steps * kMmaStep * 32; e += blockDim.x) {
+        const int L = e & 31, j = (e >> 5) % kMmaStep, st = (e >> 5) / kMmaStep;
         const int gg = L >> 2, tt = L & 3;
         uint2 v = make_uint2(0u, 0u);
         if (gg < a.nb)
-            v = *reinterpret_cast<const uint2*>(a.x + (size_t)gg * H + st * kStepK + (j >> 2) * 64 + tt * 16 +
+            v = *reinterpret_cast<const uint2*>(a.x + (size_t)gg * H + st * STEP + (j >> 2) * 64 + tt * 16 +
                                                 (j & 3) * 4);
         reinterpret_cast<uint2*>(xfrag)[e] = v;
     }
@@ -174,16 +181,19 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     bool first = true;
     const bool starts_cut = v_lo % n_steps != 0;
-    Seg w[2];
-    if (v_lo < v_hi) load_seg(w[0], unit_ptr(v_lo));
-    for (int v0 = v_lo; v0 < v_hi; v0 += 2) {
+    Seg<STEP> w[NBUF];
+    if (NBUF == 2 && v_lo < v_hi) load_seg<STEP>(w[0], unit_ptr(v_lo));
+    for (int v0 = v_lo; v0 < v_hi; v0 += NBUF) {
 #pragma unroll
-        for (int d = 0; d < 2; ++d) {
+        for (int d = 0; d < NBUF; ++d) {
             const int v = v0 + d;
             if (v < v_hi) {
-                if (v + 1 < v_hi) load_seg(w[d ^ 1], unit_ptr(v + 1));
+                if (NBUF == 1)
+                    load_seg<STEP>(w[0], unit_ptr(v));  // one step at a time: the other warps cover its latency
+                else if (v + 1 < v_hi)
+                    load_seg<STEP>(w[d ^ 1], unit_ptr(v + 1));
                 const int grp = v / n_steps, st = v % n_steps;
-                step_mma(w[d], afrag0 + (uint32_t)(st * 16 * 256), c0, c1);
+                step_mma<STEP>(w[d], afrag0 + (uint32_t)(st * kMmaStep * 256), c0, c1);
                 const bool grp_end = st + 1 == n_steps, range_end = v + 1 == v_hi;
                 if (grp_end || range_end) {
                     const float s0 = c0[0] + c1[0], s1 = c0[1] + c1[1];
@@ -252,33 +262,12 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     }
 }
 
-}  // namespace gmma
-
-bool gemv_mma_supported(int nb, int H) {  // 1-8 hidden rows, H % 256 == 0, hidden rows fit shared memory
-    return nb >= 1 && nb <= gmma::kMaxRows && H >= gmma::kStepK && H % gmma::kStepK == 0 &&
-           (size_t)H * 16 <= 160 * 1024;
-}
-
-cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
-                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
-    using namespace gmma;
-    if (!gemv_mma_supported(nb, H) || n_rows < 1 || n_rows > INT_MAX - kRowsG) return cudaErrorNotSupported;
-    Args a{};
-    a.x = x;
-    a.W = W;
-    a.cand = cand;
-    a.nb = nb;
-    a.H = H;
-    a.n_rows = n_rows;
-    a.n_groups = (n_rows + kRowsG - 1) / kRowsG;
-    a.ws = ws;
-    a.err = ws.ticket + 1;
-    a.ids = ids;
-    a.maxlogit = maxlogit;
-    a.tail = tail;
-    const size_t smem = (size_t)H * 16;
+template <int STEP, int NBUF>
+static cudaError_t launch_steps(const Args& a, cudaStream_t s) {
+    auto kernel = k_gemv_mma_bf16<STEP, NBUF>;
+    const size_t smem = (size_t)a.H * 16;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemv_mma_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     static std::mutex mu;
@@ -292,7 +281,7 @@ cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_
         if (it != cache.end()) {
             per_sm = it->second;
         } else {
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_mma_bf16, kThreadsG, smem);
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreadsG, smem);
             if (e != cudaSuccess) return e;
             cache[key] = per_sm;
         }
@@ -310,7 +299,36 @@ cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_gemv_mma_bf16, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace gmma
+
+bool gemv_mma_supported(int nb, int H) {  // 1-8 hidden rows, H % 256 == 0, hidden rows fit shared memory
+    return nb >= 1 && nb <= gmma::kMaxRows && H >= gmma::kStepK && H % gmma::kStepK == 0 &&
+           (size_t)H * 16 <= 160 * 1024;
+}
+
+cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                                 bool long_steps) {
+    using namespace gmma;
+    if (!gemv_mma_supported(nb, H) || n_rows < 1 || n_rows > INT_MAX - kRowsG) return cudaErrorNotSupported;
+    Args a{};
+    a.x = x;
+    a.W = W;
+    a.cand = cand;
+    a.nb = nb;
+    a.H = H;
+    a.n_rows = n_rows;
+    a.n_groups = (n_rows + kRowsG - 1) / kRowsG;
+    a.ws = ws;
+    a.err = ws.ticket + 1;
+    a.ids = ids;
+    a.maxlogit = maxlogit;
+    a.tail = tail;
+    if (long_steps && H % kStepLong == 0) return launch_steps<kStepLong, 1>(a, s);
+    return launch_steps<kStepK, 2>(a, s);
 }
 
 }  // namespace vh

@@ -44,8 +44,11 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
 // gemv_mma_supported: H % 256 == 0 and the hidden rows (16*H bytes in
 // fragment order) fit shared memory.  Returns cudaErrorNotSupported otherwise.
 bool gemv_mma_supported(int nb, int H);
+// long_steps: 512-element steps (1 KiB of each head row per load step, one
+// step in registers) when H % 512 == 0, else 256-element steps, two in flight.
 cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
-                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
+                                 Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                                 bool long_steps = false);
 // One launch group (nb <= gemv_group(H) hidden rows) of the bf16 draft head:
 // the kernel both draft entry points use for that group size.
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
