@@ -568,7 +568,8 @@ def measure_tiny(torch, vh, synth, timer):
             "draft_ids_equal_oracle": f"{ids_ok}/3",
             "verify_next_ids_equal_oracle": f"{int((nid.cpu().numpy() == o_nid).sum())}/4",
             "accept_len": int(acc.item()), "oracle_accept_len": int(o_acc),
-            "draft_call_us": stats(us_d), "verify_call_us": stats(us_v)}
+            "draft_call_us": stats(us_d), "verify_call_us": stats(us_v),
+            "kernels": "draft and verify k_gemv_mma_bf16 (warp MMAs fed from the weight stream)"}
 
 
 def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core=True):

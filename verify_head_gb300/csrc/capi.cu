@@ -71,10 +71,17 @@ cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t*
     // holds.  One row: the CUDA-core GEMV on tables under 512 MiB (it starts faster: 256 MiB 45.5 against
     // 47.8 us, 384 MiB 69.7 against 70.0 us per chained call), the warp MMAs from 512 MiB up (88.2 against
     // 89.8 us; the 248,320 x 2048 head 160.5-161.3 against 167.2 us, 0.93 against 0.90 of HBM)
+    // One row of 256 or 512 elements: the warp MMAs at every table size, where a 512- or 1024-byte row
+    // leaves the GEMV too few bytes in flight per warp (262,144 x 256: 28.6 against 55.3 us; 131,072 x
+    // 512: 28.4 against 31.6 us; 1,024 x 256: 6.5 against 7.2 us per chained call).
     constexpr long long kOneRowMmaBytes = 512ll << 20;
     const long long bytes = (long long)n_rows * H * 2;
-    if (gemv_mma_supported(nb, H) && (nb >= 2 || bytes >= kOneRowMmaBytes))
-        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s, long_steps(nb, bytes));
+    // At H = 512 a one-row draft takes 512-element steps: a row group is then one unit of work, never cut
+    // between warps, so a row scores the same bits wherever it sits in the table, as on the GEMV; they are
+    // also faster there (131,072 x 512: 28.4 against 28.7 us; 990,000 x 512: 164.6 against 170.0 us).
+    if (gemv_mma_supported(nb, H) && (nb >= 2 || H <= 512 || bytes >= kOneRowMmaBytes))
+        return launch_gemv_mma_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s,
+                                    long_steps(nb, bytes) || (nb == 1 && H == 512));
     return launch_gemv_bf16(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, tail, s);
 }
 
