@@ -4,9 +4,10 @@ One bench step = one MTP3 draft chain on the single-stream decode workload:
 three sequential draft-head calls (B = 1, a fresh hidden vector each) on a
 65,536-row x 2048 bf16 candidate head drawn from the 248,320-row output head.
 `value` is draft steps/s (3 calls per bench step) measured on the device with
-CUDA events around each call, with L2 flushed (256 MiB write) before every
-call and outside the timed events, so every call reads the 268 MB head from
-HBM.  The same run also measures (reported under "verify", "sweep" and
+CUDA events around each call, with L2 flushed before every call and outside
+the timed events (a 256 MiB write, then a 256 MiB read so that the write's
+dirty lines go back to HBM before the start event, not inside the timed
+call), so every call reads the 268 MB head from HBM.  The same run also measures (reported under "verify", "sweep" and
 "nvfp4"): the batched greedy verify (64 x 4 rows against the full head), the
 head-size sweep (248,320 / 65,536 / 32,768 rows) and the 4-bit head
 (65,536 x 4096, B = 1 and 8).
@@ -172,16 +173,26 @@ class Timer:
     """Per-call device time with CUDA events on the current stream; L2 is
     flushed before each call, outside the events."""
 
-    def __init__(self, torch, flush=True):
+    def __init__(self, torch, flush=True, clean=True):
         self.torch = torch
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush else None
+        # read after the write: it evicts the write's dirty lines (written back to HBM here, outside the
+        # events) and leaves L2 holding clean lines of a buffer the timed call never touches
+        self.clean_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda") if flush and clean \
+            else None
+        self.sink = torch.empty(1, dtype=torch.float32, device="cuda")
 
     def flush(self):
-        """Evict L2 (256 MiB write), then queue ~100 us of GPU sleep so that
-        the host has enqueued the timed call before its start event runs:
-        the events then bracket device time only, not host launch latency."""
+        """Evict L2 (256 MiB write, then a 256 MiB read), then queue ~100 us
+        of GPU sleep so that the host has enqueued the timed call before its
+        start event runs: the events then bracket device time only, not host
+        launch latency.  Without the read, up to an L2's worth of the write's
+        dirty lines is written back while the timed call streams its head,
+        which took the headline chain from 41.8 to 45.5 us per call."""
         if self.flush_buf is not None:
             self.flush_buf.fill_(1)
+        if self.clean_buf is not None:
+            self.torch.sum(self.clean_buf, dim=0, keepdim=True, out=self.sink)
         self.torch.cuda._sleep(PREROLL_CYCLES)
 
     def time_calls(self, fn, n, warmup=3):
@@ -328,6 +339,12 @@ def run_ours(args):
         warm_evs.append((a, b))
     torch.cuda.synchronize()
     warm_st = stats([a.elapsed_time(b) * 1e3 / 3 for a, b in warm_evs])
+    # the same chain after a write-only flush: the write's dirty lines stay in L2 and go back to HBM
+    # while the chain streams its head; reported beside the value for comparison, never as it
+    wo_timer = Timer(torch, clean=False)
+    wo_st = stats([t / 3 for t in wo_timer.time_calls(lambda: [call(i) for i in range(3)],
+                                                      max(10, args.steps // 10))])
+    del wo_timer
     total_s = sum(per_step) * 1e-6
     if world > 1:
         t = torch.tensor([total_s], dtype=torch.float64, device=dev)
@@ -425,13 +442,16 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generators; no corpus or trained weights)",
         "config": {"workload": WORKLOAD, "Vc": case.Vc, "H": case.H, "B": case.B, "draft_steps_per_step": 3,
-                   "l2": "flushed before every call (256 MiB write outside the timed events)",
+                   "l2": "flushed before every chain outside the timed events: a 256 MiB write, then a 256 MiB "
+                         "read, so that no dirty flush lines are written back inside the timed region",
                    "timing": "CUDA events around each 3-call chain on the launching stream (L2 flushed before "
                              "each chain); a ~100 us sleep kernel is queued before the start event so host "
                              "launch latency is not timed",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "draft_call_us": st,
         "draft_call_us_warm": {**warm_st, "what": "the same 3-call chain without the L2 flush between chains"},
+        "draft_call_us_write_only_flush": {**wo_st, "what": "the same 3-call chain after a 256 MiB write alone "
+                                                            "(its dirty lines are written back inside the chain)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_src,
                      "frac_of_8000_spec": round(achieved / 8000.0, 4),
