@@ -89,7 +89,7 @@ VH_API size_t vh_workspace_bytes(int rows);
  *  B         1 <= B <= 256 (processed in groups of 8 hidden rows; each group
  *            reads W_cand once: 2-8 rows on warp-level MMAs when H % 256 ==
  *            0, one row on the streaming GEMV, or on the warp-level MMAs
- *            when H is 256 or 512 or the table is 512 MiB or more)
+ *            when H is 256 or 512 or the table is 384 MiB or more)
  *  H         16 <= H <= 65536, H % 16 == 0
  *  Vc        1 <= Vc <= 2^31 - 1
  *  ids       device, int32 [B] (out)

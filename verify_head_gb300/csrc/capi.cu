@@ -67,14 +67,15 @@ static bool long_steps(int nb, long long head_bytes) {
 
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
-    // 2-8 rows: the warp MMAs (0.81-0.82 of HBM on 65,536 x 2048), where the GEMV slows with every row it
-    // holds.  One row: the CUDA-core GEMV on tables under 512 MiB (it starts faster: 256 MiB 45.5 against
-    // 47.8 us, 384 MiB 69.7 against 70.0 us per chained call), the warp MMAs from 512 MiB up (88.2 against
-    // 89.8 us; the 248,320 x 2048 head 160.5-161.3 against 167.2 us, 0.93 against 0.90 of HBM)
+    // 2-8 rows: the warp MMAs (0.85-0.87 of HBM on 65,536 x 2048), where the GEMV slows with every row it
+    // holds.  One row: the CUDA-core GEMV on tables under 384 MiB (it starts faster: 128 MiB 22.6 against
+    // 26.3 us, 256 MiB 41.2 against 45.3 us per chained call), the warp MMAs from 384 MiB up (65.2 against
+    // 65.7 us; 512 MiB 83.8 against 86.7 us; the 248,320 x 2048 head 150.6 against 161.0 us, 0.99 against
+    // 0.93 of HBM)
     // One row of 256 or 512 elements: the warp MMAs at every table size, where a 512- or 1024-byte row
     // leaves the GEMV too few bytes in flight per warp (262,144 x 256: 28.6 against 55.3 us; 131,072 x
     // 512: 28.4 against 31.6 us; 1,024 x 256: 6.5 against 7.2 us per chained call).
-    constexpr long long kOneRowMmaBytes = 512ll << 20;
+    constexpr long long kOneRowMmaBytes = 384ll << 20;
     const long long bytes = (long long)n_rows * H * 2;
     // At H = 512 a one-row draft takes 512-element steps: a row group is then one unit of work, never cut
     // between warps, so a row scores the same bits wherever it sits in the table, as on the GEMV; they are
