@@ -8,17 +8,19 @@
 // MMA roles.  mma.m16n8k16 with A = the hidden rows (M = 16: up to 8 real
 // rows, the upper 8 are zero), B = 8 head rows (N = 8), fp32 accumulation.
 // Lane L (g = L/4, t = L%4) supplies B for head row g of the group, so a warp
-// streams 8 head rows at once, 512 contiguous bytes of each per step: load i
-// (i = 0..3) of lane t reads the row's bytes 128i + 32t .. +31, so the four
-// lanes of a row read one whole 128-byte line per instruction.
+// streams 8 head rows at once, STEP contiguous elements of each per step: load
+// i (i < STEP/64) of lane t reads the row's bytes 128i + 32t .. +31, so the
+// four lanes of a row read one whole 128-byte line per instruction.  A step is
+// 256 elements (512 bytes of each row, two steps in flight per warp) or 512
+// elements (1 KiB of each row, one step in flight).
 //
-// K order.  Within a 256-element step, MMA j = 4i + m (i, m = 0..3) gives lane
+// K order.  Within a step, MMA j = 4i + m (i < STEP/64, m = 0..3) gives lane
 // (g, t) the physical elements 64i + 16t + 4m + {0,1} for its K slots {2t,
 // 2t+1} and 64i + 16t + 4m + {2,3} for {2t+8, 2t+9}, on A and B alike: each
 // MMA sums the same products as the plain order, and a lane's B registers for
 // MMA j are registers 2m and 2m+1 of its load i.  The hidden rows sit in
 // shared memory in that fragment order: lane L's 8 bytes for (step s, MMA j)
-// are row g's elements 256s + 64i + 16t + 4m .. +3, and a warp reads 256
+// are row g's elements STEP*s + 64i + 16t + 4m .. +3, and a warp reads 256
 // consecutive bytes per MMA.
 //
 // Output.  Accumulator registers c0 / c1 of lane (g, t) are hidden row g's
@@ -29,8 +31,9 @@
 // acceptance scan and re-zeroes the workspace.
 //
 // Work split.  Each CTA owns whole 8-row groups; inside a CTA the (group,
-// 256-element step) units are split evenly over the warps, and a group cut
-// between two warps is summed in shared memory in warp order.
+// step) units are split evenly over the warps, and a group cut between two
+// warps is summed in shared memory in warp order (with one step per group,
+// no group is ever cut: a row then scores the same bits wherever it sits).
 #include <algorithm>
 #include <climits>
 #include <map>
