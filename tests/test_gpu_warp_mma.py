@@ -77,6 +77,18 @@ def test_draft_full_size_65536x2048(vh, orc, syn, B):
     check_draft(vh, orc, case.hidden[0], case.W, case.cand_ids)
 
 
+def test_draft_long_steps_on_a_768_mib_table(vh, orc, syn):
+    """2-8 rows against a table of 768 MiB or more take the 512-element steps
+    (1 KiB of each head row per load step): 4 rows on 201,003 x 2048 (785 MiB,
+    a ragged last 8-row group) against the oracle."""
+    Vc, H, B = 201_003, 2048, 4
+    cand = syn.sorted_subset(61, 2, 2_000_000, Vc)
+    W = syn.normal_bf16(62, 1, (Vc, H), 0.02)
+    x = syn.normal_bf16(63, 3, (B, H), 1.0)
+    assert Vc * H * 2 >= 768 << 20
+    check_draft(vh, orc, x, W, cand)
+
+
 def test_draft_ties_across_group_warp_and_cta_boundaries(vh, syn):
     """One winning row planted at many places (both sides of 8-row group
     boundaries, scattered over the table so that warp ranges and CTA ranges
