@@ -646,7 +646,7 @@ def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core
         nbytes_r = vc.W.nbytes + R * 2048 * 2
         rows[str(R)] = {"rounds_per_s": round(1e6 / med, 1), "median_us": round(med, 2),
                         "hbm_frac": round(nbytes_r / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                        "kernel": ("k_gemv_mma_bf16 (warp MMAs, 1 KiB steps)" if R <= 8 else
+                        "kernel": ("k_gemv_mma_bf16 (warp MMAs, 1 KiB steps)" if R <= 16 else
                                    "k_verify_tc (one CTA)" if R <= 128 else "k_verify_tc2 (CTA pair)")}
     out["verify_rows"] = rows
     del Wf, X
@@ -684,15 +684,15 @@ def measure_sweep(torch, vh, synth, timer, peaks):
 
 
 def measure_draft_batch(torch, vh, synth, timer, peaks):
-    """The bf16 draft head 65,536 x 2048 for 2 / 4 / 8 hidden rows per call
-    (warp-level MMAs fed from the weight stream): three draft steps per chain
-    as in the bench step, per call = chain / 3."""
+    """The bf16 draft head 65,536 x 2048 for 2 / 4 / 8 / 16 hidden rows per
+    call (warp-level MMAs fed from the weight stream, one pass each): three
+    draft steps per chain as in the bench step, per call = chain / 3."""
     dev = torch.device("cuda")
-    c = synth.draft_case(Vc=65_536, H=2048, B=8, steps=3, seed=2)
+    c = synth.draft_case(Vc=65_536, H=2048, B=16, steps=3, seed=2)
     Wc = torch.from_numpy(c.W.view(np.int16)).to(dev).view(torch.bfloat16)
     cc = torch.from_numpy(c.cand_ids).to(dev)
     out = {}
-    for B in (2, 4, 8):
+    for B in (2, 4, 8, 16):
         xs = [torch.from_numpy(np.ascontiguousarray(h[:B]).view(np.int16)).to(dev).view(torch.bfloat16)
               for h in c.hidden]
         wsb = vh.workspace(B)

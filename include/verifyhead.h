@@ -86,10 +86,11 @@ VH_API size_t vh_workspace_bytes(int rows);
  *            of the candidate rows, not a view of the full head)
  *  cand_ids  device, int32 [Vc], ascending and distinct (precondition, not
  *            checked; ties are broken by id either way), values in [0, 2^31)
- *  B         1 <= B <= 256 (processed in groups of 8 hidden rows; each group
- *            reads W_cand once: 2-8 rows on warp-level MMAs when H % 256 ==
- *            0, one row on the streaming GEMV, or on the warp-level MMAs
- *            when H is 256 or 512 or the table is 384 MiB or more)
+ *  B         1 <= B <= 256 (processed in groups of 16 hidden rows when H %
+ *            256 == 0 and H <= 5120, else of 8; each group reads W_cand
+ *            once: 2-16 rows on warp-level MMAs when H % 256 == 0, one row
+ *            on the streaming GEMV, or on the warp-level MMAs when H is 256
+ *            or 512 or the table is 384 MiB or more)
  *  H         16 <= H <= 65536, H % 16 == 0
  *  Vc        1 <= Vc <= 2^31 - 1
  *  ids       device, int32 [B] (out)
@@ -191,8 +192,9 @@ VH_API vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* 
  *  ws            device workspace, ws_bytes >= vh_workspace_bytes(B*(k+1))
  *
  * Rows are processed in groups of at most 256 on the tensor cores (H % 64
- * == 0; up to 8 rows on warp-level MMAs when H % 256 == 0 and H <= 10240)
- * or 8 on CUDA cores (other H); each group reads W_full once.
+ * == 0; up to 16 rows on warp-level MMAs when H % 256 == 0 and H <= 5120,
+ * up to 8 when 5120 < H <= 10240) or 8 on CUDA cores (other H); each group
+ * reads W_full once.
  */
 VH_API vh_status spec_verify_greedy(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k, int H,
                              int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
@@ -293,12 +295,12 @@ VH_API vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq,
 
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
-    VH_PATH_AUTO = 0,      /* 1-8 rows, H % 256 == 0 and H <= 10240: VH_PATH_WARP_MMA;
-                              else tcgen05 when H % 64 == 0, else CUDA cores */
+    VH_PATH_AUTO = 0,      /* 1-16 rows, H % 256 == 0 and H <= 5120 (1-8 rows up to H = 10240):
+                              VH_PATH_WARP_MMA; else tcgen05 when H % 64 == 0, else CUDA cores */
     VH_PATH_CUDA_CORE = 1, /* streaming GEMV, groups of 8 rows */
     VH_PATH_TENSOR = 2,    /* tcgen05 skinny GEMM, groups of 256 rows; VH_ERR_SHAPE if H % 64 != 0 */
-    VH_PATH_WARP_MMA = 3   /* warp-level MMAs fed from the weight stream, groups of 8 rows; VH_ERR_SHAPE
-                              unless H % 256 == 0 and H <= 10240 */
+    VH_PATH_WARP_MMA = 3   /* warp-level MMAs fed from the weight stream, groups of 16 rows (8 when
+                              H > 5120); VH_ERR_SHAPE unless H % 256 == 0 and H <= 10240 */
 } vh_path;
 
 /* spec_verify_greedy with an explicit kernel choice (same results up to fp32

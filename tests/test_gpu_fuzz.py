@@ -124,14 +124,15 @@ def test_fuzz_verify_bf16(vh, orc, syn, case):
 
 @pytest.mark.parametrize("case", range(8 * SCALE))
 def test_fuzz_warp_mma_bf16(vh, orc, syn, case):
-    """The bf16 head on warp-level MMAs: the draft at 2-8 rows (its default
-    for widths that are multiples of 256) and the verify on VH_PATH_WARP_MMA
-    (one or several 8-row passes), at every width it takes up to 10,240."""
+    """The bf16 head on warp-level MMAs: the draft at 2-16 rows (its default
+    for widths that are multiples of 256; 9-16 rows in one pass up to H =
+    5,120, in 8-row passes above) and the verify on VH_PATH_WARP_MMA (one or
+    several passes of up to 16 rows), at every width it takes up to 10,240."""
     import torch
     rng = np.random.default_rng(1400 + case)
     H = 256 * int(rng.integers(1, 41))  # 256 .. 10,240
     if case % 2 == 0:
-        B = int(rng.integers(2, 9))
+        B = int(rng.integers(2, 17))
         Vc = _rows_for(rng, MAC_BUDGET, B * H)
         W = syn.normal_bf16(10_000 + case, 1, (Vc, H), 0.02)
         cand = syn.sorted_subset(10_000 + case, 2, 248_320, Vc)

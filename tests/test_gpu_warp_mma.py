@@ -1,7 +1,7 @@
 """The bf16 head on warp-level MMAs fed from the weight stream (k_gemv_mma_bf16):
-the draft head for 2-8 hidden rows (its default there) and greedy verify (on
-VH_PATH_WARP_MMA, and under AUTO for up to 8 rows), against the CPU oracle
-through the C ABI."""
+the draft head for 2-16 hidden rows (its default there; 9-16 rows need H <=
+5120) and greedy verify (on VH_PATH_WARP_MMA, and under AUTO for up to 16
+rows), against the CPU oracle through the C ABI."""
 import os
 
 import numpy as np
@@ -60,10 +60,12 @@ def check_draft(vh, orc, x, W, cand):
 
 
 # 8-row groups: Vc = 1 / 7 / 8 / 9 cover one partial group, exactly one, one plus one row; the widest H
-# the kernel takes is 10,240 (its hidden rows fill 160 KiB of shared memory)
+# the kernel takes is 10,240 for up to 8 hidden rows and 5,120 for 9-16 (the hidden rows fill 160 KiB of
+# shared memory); past 5,120 a batch of 9-16 runs as groups of 8 (and past 10,240 on the CUDA-core GEMV)
 @pytest.mark.parametrize("Vc,H,B", [(1, 256, 2), (7, 256, 3), (8, 512, 8), (9, 512, 5), (1001, 1024, 8),
                                     (20_011, 2048, 2), (3000, 4096, 8), (700, 8192, 4), (500, 10240, 3),
-                                    (300, 10496, 2)])
+                                    (300, 10496, 2), (9, 256, 9), (1001, 1024, 12), (20_011, 2048, 16),
+                                    (3000, 5120, 16), (600, 5376, 13), (4097, 512, 24)])
 def test_draft_shapes(vh, orc, syn, Vc, H, B):
     cand = syn.sorted_subset(Vc + H + 3, 2, 300_000, Vc)
     W = syn.normal_bf16(Vc + 17, 1, (Vc, H), 0.02)
@@ -71,7 +73,7 @@ def test_draft_shapes(vh, orc, syn, Vc, H, B):
     check_draft(vh, orc, x, W, cand)
 
 
-@pytest.mark.parametrize("B", [2, 8])
+@pytest.mark.parametrize("B", [2, 8, 16])
 def test_draft_full_size_65536x2048(vh, orc, syn, B):
     case = syn.draft_case(Vc=65_536, H=2048, B=B, steps=1, seed=2)
     check_draft(vh, orc, case.hidden[0], case.W, case.cand_ids)
@@ -94,13 +96,13 @@ def test_draft_ties_across_group_warp_and_cta_boundaries(vh, syn):
     boundaries, scattered over the table so that warp ranges and CTA ranges
     cut between copies, and the last row): every hidden row must return the
     lowest candidate id among the copies, with the copies' exact score."""
-    Vc, H, B = 65_536, 256, 8
+    Vc, H, B = 65_536, 256, 16
     W = syn.normal_bf16(41, 1, (Vc, H), 0.02)
-    x = syn.normal_bf16(42, 3, (B, H), 1.0)
+    # non-negative hidden rows (sign bits cleared) and an all-ones winner: every hidden row scores it
+    # sum |x| ~ 200, far above the rest (~1); 16 rows use the upper half of the MMA's A operand as well
+    x = syn.normal_bf16(42, 3, (B, H), 1.0) & np.uint16(0x7FFF)
     cand = syn.sorted_subset(43, 2, 248_320, Vc)
-    # the winner: the sign pattern of the hidden rows' sum, scaled up (every row scores it far above the rest)
-    s = x.view(np.int16).astype(np.int32)
-    sign = np.where(np.sum(np.where(s < 0, -1, 1), axis=0) < 0, 0xBF80, 0x3F80).astype(np.uint16)  # -1 / +1
+    sign = np.full(H, 0x3F80, np.uint16)  # +1
     planted = sorted({7, 8, 15, 16, 255, 256, 431, 432, 1023, 1024, 4095, 4096, 8191, 8192, 12_345, 20_000,
                       32_767, 32_768, 40_960, 50_001, 65_528, 65_535})
     for r in planted:
@@ -142,9 +144,10 @@ def check_verify(vh, orc, syn, X, W, B, k, path, seed):
     check_accept(g_acc, g_nid, o_acc, o_ml, o_sec, draft, B, k)
 
 
-# VH_PATH_WARP_MMA: 2-8 rows in one pass, 12 rows in two
+# VH_PATH_WARP_MMA: 2-16 rows in one pass (8 per pass past H = 5120), 20 rows in two
 @pytest.mark.parametrize("B,k,V,H", [(1, 3, 5000, 256), (2, 3, 3001, 512), (1, 7, 2049, 1024), (1, 1, 777, 2048),
-                                     (1, 3, 40_000, 4096), (3, 3, 1500, 256), (1, 3, 9, 512)])
+                                     (1, 3, 40_000, 4096), (3, 3, 1500, 256), (1, 3, 9, 512), (4, 3, 20_000, 2048),
+                                     (1, 15, 3001, 1024), (3, 2, 1000, 6144), (5, 3, 2500, 512)])
 def test_verify_shapes(vh, orc, syn, B, k, V, H):
     path = vh.VH_PATH_WARP_MMA
     W = syn.normal_bf16(V + H + 5, 1, (V, H), 0.02)
@@ -152,8 +155,9 @@ def test_verify_shapes(vh, orc, syn, B, k, V, H):
     check_verify(vh, orc, syn, X, W, B, k, path, seed=B * 100 + k + 1)
 
 
-# AUTO takes the warp MMAs for up to 8 rows (H % 256 == 0)
-@pytest.mark.parametrize("B,k,V,H", [(1, 3, 4096, 256), (2, 3, 20_000, 512), (1, 7, 3001, 2048)])
+# AUTO takes the warp MMAs for up to 16 rows (H % 256 == 0, H <= 5120 above 8 rows)
+@pytest.mark.parametrize("B,k,V,H", [(1, 3, 4096, 256), (2, 3, 20_000, 512), (1, 7, 3001, 2048), (4, 3, 9000, 1024),
+                                     (3, 3, 5000, 5120)])
 def test_verify_auto_small_heads(vh, orc, syn, B, k, V, H):
     W = syn.normal_bf16(V + H + 9, 1, (V, H), 0.02)
     X = syn.normal_bf16(B + k + 13, 4, (B * (k + 1), H), 1.0)
@@ -186,11 +190,11 @@ def _load_verify_golden():
     return rows, seqs, meta
 
 
-@pytest.mark.parametrize("n_seq", [1, 2])
+@pytest.mark.parametrize("n_seq", [1, 2, 3, 4])
 def test_batch1_verify_full_head_against_stored_oracle(vh, orc, syn, n_seq):
-    """The batch-1 (and batch-2) MTP3 verify on the warp-MMA path against the
+    """The batch-1 to batch-4 MTP3 verify on the warp-MMA path against the
     full 248,320 x 2048 head: the first sequences of the stored full-size
-    oracle results (4 or 8 rows)."""
+    oracle results (4, 8, 12 or 16 rows)."""
     rows, seqs, meta = _load_verify_golden()
     case = syn.verify_case(B=64, k=3, H=2048, V=syn.V_FULL, seed_w=2, seed=4, with_head=True)
     assert syn.fingerprint(case.X) == int(meta["fingerprint_x"][0])

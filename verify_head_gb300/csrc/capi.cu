@@ -15,7 +15,7 @@ using vh::gemv_group;
 using vh::kMaxDraftB;
 using vh::kMaxH;
 constexpr int kTcRows = 256;   // hidden rows per tensor-core verify launch
-constexpr int kMmaRows = 8;    // hidden rows per warp-MMA launch
+constexpr int kMmaRows = 16;   // hidden rows per warp-MMA launch (8 when H > 5120)
 constexpr int kTcFp4Rows = 16;  // hidden rows per tensor-core 4-bit draft launch
 constexpr int kMmaFp4Rows = 8;  // hidden rows per warp-level-MMA 4-bit launch
 constexpr int kPackedRows = 16;  // hidden rows per pass over a tiled 4-bit head
@@ -65,10 +65,12 @@ static bool long_steps(int nb, long long head_bytes) {
     return nb >= 2 && head_bytes >= kLongStepBytes;
 }
 
+int draft_group(int H) { return gemv_mma_supported(16, H) ? 16 : gemv_group(H); }
+
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
-    // 2-8 rows: the warp MMAs (0.85-0.87 of HBM on 65,536 x 2048), where the GEMV slows with every row it
-    // holds.  One row: the CUDA-core GEMV on tables under 384 MiB (it starts faster: 128 MiB 22.6 against
+    // 2-16 rows: the warp MMAs (0.85-0.87 of HBM on 65,536 x 2048 at 2-8 rows), where the GEMV slows with
+    // every row it holds.  One row: the CUDA-core GEMV on tables under 384 MiB (it starts faster: 128 MiB 22.6 against
     // 26.3 us, 256 MiB 41.2 against 45.3 us per chained call), the warp MMAs from 384 MiB up (65.2 against
     // 65.7 us; 512 MiB 83.8 against 86.7 us; the 248,320 x 2048 head 150.6 against 161.0 us, 0.99 against
     // 0.93 of HBM)
@@ -129,7 +131,7 @@ vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const vh::Workspace w = make_ws(ws, B);
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
-    const int grp = gemv_group(H);
+    const int grp = vh::draft_group(H);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
         cudaError_t e = vh::launch_draft_group(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),
@@ -245,7 +247,8 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     const bool wmma = (path == VH_PATH_WARP_MMA) ||
                       (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H));
     const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
-    const int group = wmma ? kMmaRows : tensor ? kTcRows : gemv_group(H);
+    const int mma_group = vh::gemv_mma_supported(kMmaRows, H) ? kMmaRows : 8;  // 16 rows need H <= 5120
+    const int group = wmma ? mma_group : tensor ? kTcRows : gemv_group(H);
     for (int r0 = 0; r0 < R; r0 += group) {
         const int nr = std::min(group, R - r0);
         vh::AcceptTail tail;

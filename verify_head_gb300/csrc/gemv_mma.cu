@@ -6,7 +6,8 @@
 // (the target scores k+1 rows against the full head).
 //
 // MMA roles.  mma.m16n8k16 with A = the hidden rows (M = 16: up to 8 real
-// rows, the upper 8 are zero), B = 8 head rows (N = 8), fp32 accumulation.
+// rows with the upper 8 zero, or up to 16 in the 16-row instance), B = 8 head
+// rows (N = 8), fp32 accumulation.
 // Lane L (g = L/4, t = L%4) supplies B for head row g of the group, so a warp
 // streams 8 head rows at once, STEP contiguous elements of each per step: load
 // i (i < STEP/64) of lane t reads the row's bytes 128i + 32t .. +31, so the
@@ -21,12 +22,15 @@
 // MMA j are registers 2m and 2m+1 of its load i.  The hidden rows sit in
 // shared memory in that fragment order: lane L's 8 bytes for (step s, MMA j)
 // are row g's elements STEP*s + 64i + 16t + 4m .. +3, and a warp reads 256
-// consecutive bytes per MMA.
+// consecutive bytes per MMA.  The 16-row instance also holds hidden row g+8's
+// 4 elements: 16 bytes per lane per MMA, {row g, row g+8, row g, row g+8} as
+// the A registers a0..a3 want them, 512 consecutive bytes per warp.
 //
 // Output.  Accumulator registers c0 / c1 of lane (g, t) are hidden row g's
-// scores of head rows 2t and 2t+1 of the group; c2 / c3 belong to the zero
-// rows.  Each lane keeps one packed (score, id) key for its hidden row; the
-// four lanes of a row, the warps of a CTA and the CTAs merge by max, and the
+// scores of head rows 2t and 2t+1 of the group; c2 / c3 are hidden row g+8's
+// (zero rows in the 8-row instance).  Each lane keeps one packed (score, id)
+// key per hidden row it holds; the four lanes of a row, the warps of a CTA
+// and the CTAs merge by max, and the
 // last CTA (ticket counter) writes ids / max logits, runs the optional
 // acceptance scan and re-zeroes the workspace.
 //
@@ -39,6 +43,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "vh_kernels.h"
 #include "vh_ptx.cuh"
@@ -51,7 +56,7 @@ constexpr int kThreadsG = kWarpsG * 32;
 constexpr int kStepK = 256;   // elements of K per step, short steps (512 bytes of each head row)
 constexpr int kStepLong = 512;  // long steps (1 KiB of each head row), single-buffered
 constexpr int kRowsG = 8;     // head rows per warp group (MMA N)
-constexpr int kMaxRows = 8;   // hidden rows per launch
+constexpr int kMaxRows = 16;  // hidden rows per launch (the 16-row instance)
 
 struct Args {
     const uint16_t* x;  // bf16 [nb][H]
@@ -75,14 +80,20 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     return v;
 }
 
-// D += A (16 x 16 bf16, rows g / g+8) * B (16 x 8 bf16), fp32 accumulate; the
-// rows g+8 of A are zero.
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// D += A (16 x 16 bf16: a0 / a2 row g, a1 / a3 row g+8) * B (16 x 8 bf16), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 template <int STEP>
@@ -96,26 +107,33 @@ __device__ __forceinline__ void load_seg(Seg<STEP>& s, const uint16_t* p) {  // 
     for (int i = 0; i < STEP / 64; ++i) s.v[i] = ld_stream32(p + i * 64);
 }
 
-// The STEP/16 MMAs of one step: B from the lane's registers, A from shared memory.
-template <int STEP>
+// The STEP/16 MMAs of one step: B from the lane's registers, A from shared
+// memory (8 bytes per lane per MMA with NR = 8 hidden rows, 16 with NR = 16).
+template <int STEP, int NR>
 __device__ __forceinline__ void step_mma(const Seg<STEP>& w, uint32_t afrag, float (&c0)[4], float (&c1)[4]) {
 #pragma unroll
     for (int j = 0; j < STEP / 16; ++j) {
-        const uint2 a = lds64(afrag + (uint32_t)(j * 256));
         const uint32_t b0 = w.v[j >> 2].v[2 * (j & 3)], b1 = w.v[j >> 2].v[2 * (j & 3) + 1];
-        if (j & 1)
-            mma_bf16_16816(c1, a.x, a.y, b0, b1);
-        else
-            mma_bf16_16816(c0, a.x, a.y, b0, b1);
+        if constexpr (NR == 8) {
+            const uint2 a = lds64(afrag + (uint32_t)(j * 256));
+            mma_bf16_16816((j & 1) ? c1 : c0, a.x, 0u, a.y, 0u, b0, b1);
+        } else {
+            const uint4 a = lds128(afrag + (uint32_t)(j * 512));
+            mma_bf16_16816((j & 1) ? c1 : c0, a.x, a.y, a.z, a.w, b0, b1);
+        }
     }
 }
 
-// STEP: K elements per step (256 or 512); NBUF: steps in registers per warp (2 or 1).
-template <int STEP, int NBUF>
+// STEP: K elements per step (256 or 512); NBUF: steps in registers per warp (2 or 1);
+// NR: hidden rows the instance holds (8 or 16).
+template <int STEP, int NBUF, int NR>
 __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     constexpr int kMmaStep = STEP / 16;                  // MMAs per step
-    extern __shared__ __align__(16) uint8_t xfrag[];  // [H/STEP steps][STEP/16 MMAs][32 lanes][8 B]
-    __shared__ float2 cut[kWarpsG][2][32];             // partial scores of groups cut between warps
+    constexpr int kFragB = NR == 16 ? 16 : 8;            // bytes per lane per MMA
+    constexpr int KB = NR == 16 ? 2 : 1;                 // keys (hidden rows) per lane
+    extern __shared__ __align__(16) uint8_t xfrag[];  // [H/STEP steps][STEP/16 MMAs][32 lanes][kFragB B]
+    using Cut = std::conditional_t<NR == 16, float4, float2>;
+    __shared__ Cut cut[kWarpsG][2][32];                // partial scores of groups cut between warps
     __shared__ unsigned long long merge[kMaxRows];
     __shared__ unsigned int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -146,19 +164,25 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
         if (r < a.n_rows)
             for (int c = t * 64; c < H; c += 256) prefetch_l2(a.W + (size_t)r * H + c);
     };
-    // keys of one finished group (this lane: hidden row g, head rows 2t and 2t+1)
-    unsigned long long best = 0ull;
-    auto finish_group = [&](int grp, float s0, float s1) {
-        if (g >= a.nb) return;
+    // keys of one finished group (this lane: hidden rows g and, with NR = 16, g+8; head rows 2t and 2t+1)
+    unsigned long long best[KB];
+#pragma unroll
+    for (int q = 0; q < KB; ++q) best[q] = 0ull;
+    auto finish_group = [&](int grp, float4 s) {
+        if (g >= a.nb) return;  // (then g + 8 >= nb too)
         const int r0 = (G0 + grp) * kRowsG + 2 * t;
-        const float sc[2] = {s0, s1};
+        const float sc[2][2] = {{s.x, s.y}, {s.z, s.w}};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int r = r0 + h;
             if (r < a.n_rows) {
                 const uint32_t gid = a.cand ? (uint32_t)__ldg(a.cand + r) : (uint32_t)r;
-                const unsigned long long k = make_key(sc[h], gid);
-                best = k > best ? k : best;
+#pragma unroll
+                for (int q = 0; q < KB; ++q)
+                    if (g + 8 * q < a.nb) {
+                        const unsigned long long k = make_key(sc[q][h], gid);
+                        best[q] = k > best[q] ? k : best[q];
+                    }
             }
         }
     };
@@ -172,15 +196,20 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     for (int e = threadIdx.x; e < n_steps * kMmaStep * 32; e += blockDim.x) {
         const int L = e & 31, j = (e >> 5) % kMmaStep, st = (e >> 5) / kMmaStep;
         const int gg = L >> 2, tt = L & 3;
+        const size_t off = (size_t)st * STEP + (j >> 2) * 64 + tt * 16 + (j & 3) * 4;
         uint2 v = make_uint2(0u, 0u);
-        if (gg < a.nb)
-            v = *reinterpret_cast<const uint2*>(a.x + (size_t)gg * H + st * STEP + (j >> 2) * 64 + tt * 16 +
-                                                (j & 3) * 4);
-        reinterpret_cast<uint2*>(xfrag)[e] = v;
+        if (gg < a.nb) v = *reinterpret_cast<const uint2*>(a.x + (size_t)gg * H + off);
+        if constexpr (NR == 8) {
+            reinterpret_cast<uint2*>(xfrag)[e] = v;
+        } else {
+            uint2 u = make_uint2(0u, 0u);
+            if (gg + 8 < a.nb) u = *reinterpret_cast<const uint2*>(a.x + (size_t)(gg + 8) * H + off);
+            reinterpret_cast<uint4*>(xfrag)[e] = make_uint4(v.x, u.x, v.y, u.y);
+        }
     }
     __syncthreads();
 
-    const uint32_t afrag0 = ptx::smem_u32(xfrag) + (uint32_t)lane * 8u;
+    const uint32_t afrag0 = ptx::smem_u32(xfrag) + (uint32_t)lane * (uint32_t)kFragB;
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     bool first = true;
     const bool starts_cut = v_lo % n_steps != 0;
@@ -196,14 +225,16 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
                 else if (v + 1 < v_hi)
                     load_seg<STEP>(w[d ^ 1], unit_ptr(v + 1));
                 const int grp = v / n_steps, st = v % n_steps;
-                step_mma<STEP>(w[d], afrag0 + (uint32_t)(st * kMmaStep * 256), c0, c1);
+                step_mma<STEP, NR>(w[d], afrag0 + (uint32_t)(st * kMmaStep * 32 * kFragB), c0, c1);
                 const bool grp_end = st + 1 == n_steps, range_end = v + 1 == v_hi;
                 if (grp_end || range_end) {
-                    const float s0 = c0[0] + c1[0], s1 = c0[1] + c1[1];
+                    const float4 sg = make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
                     if (!(first && starts_cut) && grp_end)
-                        finish_group(grp, s0, s1);
-                    else  // a piece of a cut group: slot 0 = this warp's first group, 1 = its last
-                        cut[warp][first ? 0 : 1][lane] = make_float2(s0, s1);
+                        finish_group(grp, sg);
+                    else if constexpr (NR == 16)  // a piece of a cut group: slot 0 = this warp's first group, 1 = its last
+                        cut[warp][first ? 0 : 1][lane] = sg;
+                    else
+                        cut[warp][first ? 0 : 1][lane] = make_float2(sg.x, sg.y);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) c0[i] = c1[i] = 0.f;
                     first = false;
@@ -216,26 +247,33 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     if (v_lo < v_hi && v_hi % n_steps != 0) {
         const int jg = (v_hi - 1) / n_steps;  // CTA-local group
         if (jg * n_steps >= v_lo) {          // its first step is ours: add the pieces in warp order
-            float s0 = 0.f, s1 = 0.f;
+            float4 sg = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int ww = warp; ww < kWarpsG; ++ww) {
                 const int wl = u_begin(ww), wh = u_begin(ww + 1);
                 if (wl >= (jg + 1) * n_steps) break;
                 if (wh <= wl) continue;  // a warp without units
-                const float2 p = cut[ww][(wl / n_steps == jg) ? 0 : 1][lane];
-                s0 += p.x;
-                s1 += p.y;
+                const Cut p = cut[ww][(wl / n_steps == jg) ? 0 : 1][lane];
+                sg.x += p.x;
+                sg.y += p.y;
+                if constexpr (NR == 16) {
+                    sg.z += p.z;
+                    sg.w += p.w;
+                }
             }
-            finish_group(jg, s0, s1);
+            finish_group(jg, sg);
         }
     }
 
     // the four lanes of a hidden row, then the warps, then the CTAs
 #pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, m);
-        best = o > best ? o : best;
+    for (int q = 0; q < KB; ++q) {
+#pragma unroll
+        for (int m = 1; m <= 2; m <<= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best[q], m);
+            best[q] = o > best[q] ? o : best[q];
+        }
+        if (t == 0 && g + 8 * q < a.nb && best[q] != 0ull) atomicMax(&merge[g + 8 * q], best[q]);
     }
-    if (t == 0 && g < a.nb && best != 0ull) atomicMax(&merge[g], best);
     __syncthreads();
     if (threadIdx.x < a.nb && merge[threadIdx.x] != 0ull) atomicMax(a.ws.keys + threadIdx.x, merge[threadIdx.x]);
     __threadfence();
@@ -265,10 +303,10 @@ __global__ void __launch_bounds__(kThreadsG, 2) k_gemv_mma_bf16(const Args a) {
     }
 }
 
-template <int STEP, int NBUF>
+template <int STEP, int NBUF, int NR>
 static cudaError_t launch_steps(const Args& a, cudaStream_t s) {
-    auto kernel = k_gemv_mma_bf16<STEP, NBUF>;
-    const size_t smem = (size_t)a.H * 16;
+    auto kernel = k_gemv_mma_bf16<STEP, NBUF, NR>;
+    const size_t smem = (size_t)a.H * (NR == 16 ? 32 : 16);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -307,9 +345,9 @@ static cudaError_t launch_steps(const Args& a, cudaStream_t s) {
 
 }  // namespace gmma
 
-bool gemv_mma_supported(int nb, int H) {  // 1-8 hidden rows, H % 256 == 0, hidden rows fit shared memory
+bool gemv_mma_supported(int nb, int H) {  // 1-16 hidden rows, H % 256 == 0, hidden rows fit shared memory
     return nb >= 1 && nb <= gmma::kMaxRows && H >= gmma::kStepK && H % gmma::kStepK == 0 &&
-           (size_t)H * 16 <= 160 * 1024;
+           (size_t)H * (nb > 8 ? 32 : 16) <= 160 * 1024;
 }
 
 cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
@@ -330,8 +368,9 @@ cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_
     a.ids = ids;
     a.maxlogit = maxlogit;
     a.tail = tail;
-    if (long_steps && H % kStepLong == 0) return launch_steps<kStepLong, 1>(a, s);
-    return launch_steps<kStepK, 2>(a, s);
+    const bool l = long_steps && H % kStepLong == 0;
+    if (nb > 8) return l ? launch_steps<kStepLong, 1, 16>(a, s) : launch_steps<kStepK, 2, 16>(a, s);
+    return l ? launch_steps<kStepLong, 1, 8>(a, s) : launch_steps<kStepK, 2, 8>(a, s);
 }
 
 }  // namespace vh

@@ -39,17 +39,21 @@ cudaError_t launch_gemv_bf16(const uint16_t* x, int nb, int H, const uint16_t* W
                              Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
                              int gather_V = 0);
 
-// bf16 head for 1-8 hidden rows on warp-level MMAs fed straight from the
+// bf16 head for 1-16 hidden rows on warp-level MMAs fed straight from the
 // weight stream (mma.m16n8k16, hidden rows as A, 8 head rows as B) + argmax.
-// gemv_mma_supported: H % 256 == 0 and the hidden rows (16*H bytes in
-// fragment order) fit shared memory.  Returns cudaErrorNotSupported otherwise.
+// gemv_mma_supported: H % 256 == 0 and the hidden rows in fragment order
+// (16*H bytes for up to 8 rows, 32*H for 9-16) fit 160 KiB of shared memory.
+// Returns cudaErrorNotSupported otherwise.
 bool gemv_mma_supported(int nb, int H);
 // long_steps: 512-element steps (1 KiB of each head row per load step, one
 // step in registers) when H % 512 == 0, else 256-element steps, two in flight.
 cudaError_t launch_gemv_mma_bf16(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                  Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
                                  bool long_steps = false);
-// One launch group (nb <= gemv_group(H) hidden rows) of the bf16 draft head:
+// Hidden rows per launch group of the bf16 draft head: 16 where the warp-MMA
+// kernel takes 16 rows (H % 256 == 0, H <= 5120), else gemv_group(H).
+int draft_group(int H);
+// One launch group (nb <= draft_group(H) hidden rows) of the bf16 draft head:
 // the kernel both draft entry points use for that group size.
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s);
