@@ -80,7 +80,7 @@ def test_draft_full_size_65536x2048(vh, orc, syn, B):
 
 
 def test_draft_long_steps_on_a_768_mib_table(vh, orc, syn):
-    """2-8 rows against a table of 768 MiB or more take the 512-element steps
+    """2-16 rows against a table of 768 MiB or more take the 512-element steps
     (1 KiB of each head row per load step): 4 rows on 201,003 x 2048 (785 MiB,
     a ragged last 8-row group) against the oracle."""
     Vc, H, B = 201_003, 2048, 4

@@ -56,7 +56,7 @@ vh_status launch_status(cudaError_t e) {
 
 namespace vh {
 
-// Warp-MMA step length.  For 2-8 rows against heads of 768 MiB or more each warp streams 1 KiB of every
+// Warp-MMA step length.  For 2-16 rows against heads of 768 MiB or more each warp streams 1 KiB of every
 // row per step: 4 rows on the 248,320 x 2048 head took 166.9-168.2 against 172.0-173.9 us with 512-byte
 // steps.  Below that, and for one row at every size, 512-byte steps are as fast or faster (4 rows on 768
 // MiB: 140.1 / 140.3 us; one row on the full head: 160.0 against 161.0 us per chained call).
@@ -239,11 +239,11 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
     // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
     // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
     // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.  For up to
-    // 8 rows the warp-level MMAs fed from the weight stream go first (H % 256 == 0): they start faster
-    // than the tcgen05 kernel (no TMEM, barrier or tensor-map set-up).  A 4-row call took 0.92-0.98 of
-    // the tcgen05 time from 128 to 768 MiB (256 MiB: 54.5 against 59.4 us) and 0.99-1.00 on the
-    // 248,320 x 2048 head (166.9 against 167.3 us), and a batch-1 MTP3 round (three one-row drafts on
-    // 65,536 x 2048, then this verify) took 289.9 against 294.3 us.
+    // 16 rows (8 above H = 5120) the warp-level MMAs fed from the weight stream go first (H % 256 == 0):
+    // they start faster than the tcgen05 kernel (no TMEM, barrier or tensor-map set-up).  A 4-row call
+    // took 0.92-0.98 of the tcgen05 time from 128 to 768 MiB (256 MiB: 54.5 against 59.4 us); on the
+    // 248,320 x 2048 head 4, 8, 12 and 16 rows took 159.7-160.0 against 165.9-166.1 us, and a batch-1
+    // MTP3 round (three one-row drafts on 65,536 x 2048, then this verify) 277.7 against 292.7 us.
     const bool wmma = (path == VH_PATH_WARP_MMA) ||
                       (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H));
     const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
