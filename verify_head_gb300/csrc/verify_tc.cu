@@ -43,7 +43,7 @@ namespace tc {
 constexpr int kBlockM = 128;      // W rows per tile (MMA M)
 constexpr int kBlockK = 64;       // K per stage (one 128 B swizzle atom of bf16)
 constexpr int kMaxN = 256;        // hidden rows per launch (MMA N <= 256)
-constexpr int kMaxStagesTc = 6;    // deepest ring of any instance
+constexpr int kMaxStagesTc = 8;    // deepest ring of any instance
 constexpr int kThreadsTc = 192;
 constexpr int kEpiWarp0 = 2;
 constexpr int kStageA = kBlockM * kBlockK * 2;  // 16 KiB
@@ -729,17 +729,16 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     a.maxlogit = maxlogit;
     a.tail = tail;
     const int grid = std::max(1, std::min(sm_count(), a.n_tiles));
-    // ring depth by width: 65-128 hidden rows fit six stages (128 rows: 166.9 against
-    // 172-174 us with four); deeper rings for fewer rows measured no better (8 stages at
-    // 64 rows: 170.0 us, as with four) or worse (10 stages at 4-16 rows: 174-176 against
-    // 168-174 us), so up to 64 rows keep four
+    // ring depth by width: up to 64 hidden rows take eight stages (20 / 32 / 64 rows on the
+    // 248,320 x 2048 head: 157.7-158.1 us against 158.1-160.1 with six and 165.9-167.9 with
+    // four), 65-128 rows fit six (128 rows: 166.9 against 172-174 us with four)
     auto go = [&](auto kernel, size_t smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kernel<<<grid, kThreadsTc, smem, s>>>(map_w, map_x, a);
         return cudaGetLastError();
     };
-    if (N <= 64) return go(k_verify_tc<4, 64>, smem_bytes_tc(4, 64));
+    if (N <= 64) return go(k_verify_tc<8, 64>, smem_bytes_tc(8, 64));
     if (N <= 128) return go(k_verify_tc<6, 128>, smem_bytes_tc(6, 128));
     return go(k_verify_tc<4, 256>, smem_bytes_tc(4, 256));
 }
