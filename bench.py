@@ -646,7 +646,7 @@ def measure_verify(torch, vh, synth, timer, peaks, load_verify_golden, cuda_core
         nbytes_r = vc.W.nbytes + R * 2048 * 2
         rows[str(R)] = {"rounds_per_s": round(1e6 / med, 1), "median_us": round(med, 2),
                         "hbm_frac": round(nbytes_r / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                        "kernel": ("k_gemv_mma_bf16 (warp MMAs, 1 KiB steps)" if R <= 16 else
+                        "kernel": ("k_verify_tc (one CTA, eight-stage ring)" if R <= 64 else
                                    "k_verify_tc (one CTA)" if R <= 128 else "k_verify_tc2 (CTA pair)")}
     out["verify_rows"] = rows
     del Wf, X
@@ -717,8 +717,8 @@ def measure_mtp3_round(torch, vh, synth, timer, peaks):
     """One batch-1 MTP3 decode round as the pages run it: three draft steps on
     the 65,536 x 2048 candidate table (B = 1), each writing its id into the
     draft-id buffer, then the greedy verify of the 4 rows against the full
-    248,320 x 2048 head, which reads those ids.  AUTO kernels (the warp-MMA
-    verify) against the same round with the tcgen05 verify."""
+    248,320 x 2048 head, which reads those ids.  AUTO kernels (the tcgen05
+    verify) against the same round with the warp-MMA verify."""
     dev = torch.device("cuda")
     c = synth.draft_case(Vc=65_536, H=2048, B=1, steps=3, seed=2)
     Wc = torch.from_numpy(c.W.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -734,7 +734,7 @@ def measure_mtp3_round(torch, vh, synth, timer, peaks):
     nid = torch.empty(4, dtype=torch.int32, device=dev)
     mlv = torch.empty(4, dtype=torch.float32, device=dev)
     out = {}
-    for name, path in (("auto", vh.VH_PATH_AUTO), ("tcgen05_verify", vh.VH_PATH_TENSOR)):
+    for name, path in (("auto", vh.VH_PATH_AUTO), ("warp_mma_verify", vh.VH_PATH_WARP_MMA)):
         def rnd(path=path):
             for k in range(3):
                 vh.mtp_draft_head_argmax(xs[k], Wc, cc, ids=draft[0, k:k + 1], maxlogit=mld[k], ws=wsd)
@@ -746,7 +746,7 @@ def measure_mtp3_round(torch, vh, synth, timer, peaks):
         nbytes = 3 * (65_536 * 2048 * 2 + 65_536 * 4) + synth.V_FULL * 2048 * 2
         out[name] = {"rounds_per_s": round(1e6 / mean, 1), **stats(us),
                      "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                     "kernels": "3 x k_gemv_bf16<1> + " + ("k_gemv_mma_bf16" if name == "auto" else "k_verify_tc")}
+                     "kernels": "3 x k_gemv_bf16<1> + " + ("k_verify_tc" if name == "auto" else "k_gemv_mma_bf16")}
     out["workload"] = ("B = 1, k = 3: 3 draft calls on 65,536 x 2048 (one id each into the draft buffer) + verify "
                        "of 4 rows against 248,320 x 2048; one round between one pair of CUDA events, L2 flushed")
     del Wc, Wf

@@ -192,9 +192,9 @@ VH_API vh_status mtp_draft_head_argmax_nvfp4(const void* hidden, const uint8_t* 
  *  ws            device workspace, ws_bytes >= vh_workspace_bytes(B*(k+1))
  *
  * Rows are processed in groups of at most 256 on the tensor cores (H % 64
- * == 0; up to 16 rows on warp-level MMAs when H % 256 == 0 and H <= 5120,
- * up to 8 when 5120 < H <= 10240) or 8 on CUDA cores (other H); each group
- * reads W_full once.
+ * == 0; against a head under 384 MiB up to 16 rows on warp-level MMAs when
+ * H % 256 == 0 and H <= 5120, up to 8 when 5120 < H <= 10240) or 8 on CUDA
+ * cores (other H); each group reads W_full once.
  */
 VH_API vh_status spec_verify_greedy(const void* hidden, const void* W_full, const int32_t* draft_ids, int B, int k, int H,
                              int V, int32_t* accept_len, int32_t* next_ids, float* row_maxlogit, void* ws,
@@ -295,8 +295,9 @@ VH_API vh_status spec_verify_greedy_nvfp4(const void* hidden, const uint8_t* Wq,
 
 /* Kernel selection for spec_verify_greedy_path. */
 typedef enum {
-    VH_PATH_AUTO = 0,      /* 1-16 rows, H % 256 == 0 and H <= 5120 (1-8 rows up to H = 10240):
-                              VH_PATH_WARP_MMA; else tcgen05 when H % 64 == 0, else CUDA cores */
+    VH_PATH_AUTO = 0,      /* 1-16 rows, H % 256 == 0, H <= 5120 (1-8 rows up to H = 10240) and a
+                              head under 384 MiB: VH_PATH_WARP_MMA; else tcgen05 when H % 64 == 0,
+                              else CUDA cores */
     VH_PATH_CUDA_CORE = 1, /* streaming GEMV, groups of 8 rows */
     VH_PATH_TENSOR = 2,    /* tcgen05 skinny GEMM, groups of 256 rows; VH_ERR_SHAPE if H % 64 != 0 */
     VH_PATH_WARP_MMA = 3   /* warp-level MMAs fed from the weight stream, groups of 16 rows (8 when

@@ -1,7 +1,7 @@
 """The bf16 head on warp-level MMAs fed from the weight stream (k_gemv_mma_bf16):
 the draft head for 2-16 hidden rows (its default there; 9-16 rows need H <=
 5120) and greedy verify (on VH_PATH_WARP_MMA, and under AUTO for up to 16
-rows), against the CPU oracle through the C ABI."""
+rows against heads under 384 MiB), against the CPU oracle through the C ABI."""
 import os
 
 import numpy as np
@@ -155,7 +155,7 @@ def test_verify_shapes(vh, orc, syn, B, k, V, H):
     check_verify(vh, orc, syn, X, W, B, k, path, seed=B * 100 + k + 1)
 
 
-# AUTO takes the warp MMAs for up to 16 rows (H % 256 == 0, H <= 5120 above 8 rows)
+# AUTO takes the warp MMAs for up to 16 rows against heads under 384 MiB (H % 256 == 0, H <= 5120 above 8 rows)
 @pytest.mark.parametrize("B,k,V,H", [(1, 3, 4096, 256), (2, 3, 20_000, 512), (1, 7, 3001, 2048), (4, 3, 9000, 1024),
                                      (3, 3, 5000, 5120)])
 def test_verify_auto_small_heads(vh, orc, syn, B, k, V, H):

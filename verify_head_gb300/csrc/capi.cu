@@ -238,14 +238,18 @@ vh_status spec_verify_greedy_path(const void* hidden, const void* W_full, const 
 
     // The one-CTA tensor kernel streams the head at the same rate for 2 rows as for 128, while the
     // CUDA-core GEMV slows with every row it holds (2 / 4 / 8 rows: 257 / 360 / 602 us against 177 us
-    // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.  For up to
-    // 16 rows (8 above H = 5120) the warp-level MMAs fed from the weight stream go first (H % 256 == 0):
-    // they start faster than the tcgen05 kernel (no TMEM, barrier or tensor-map set-up).  A 4-row call
-    // took 0.92-0.98 of the tcgen05 time from 128 to 768 MiB (256 MiB: 54.5 against 59.4 us); on the
-    // 248,320 x 2048 head 4, 8, 12 and 16 rows took 159.7-160.0 against 165.9-166.1 us, and a batch-1
-    // MTP3 round (three one-row drafts on 65,536 x 2048, then this verify) 277.7 against 292.7 us.
+    // on the 248,320 x 2048 head), so AUTO takes the tensor cores whenever the width allows.  On heads
+    // under 384 MiB up to 16 rows (8 above H = 5120) take the warp-level MMAs fed from the weight stream
+    // instead (H % 256 == 0): they start faster than the tcgen05 kernel (no TMEM, barrier or tensor-map
+    // set-up).  4 rows on 2 MiB: 10.5 against 12.3 us; on 128 / 256 MiB: 32.8 / 53.5 against 34.6 /
+    // 55.4 us.  From 512 MiB the eight-stage tcgen05 ring streams faster (512 MiB: 90.1 against 98.5
+    // us; the 248,320 x 2048 head, 16 rows: 153.9 against 158.8 us), and with dependent launch a
+    // batch-1 MTP3 round (three one-row drafts on 65,536 x 2048, then this verify) takes 269.5 against
+    // 274.0 us.
+    constexpr long long kMmaVerifyMaxBytes = 384ll << 20;
     const bool wmma = (path == VH_PATH_WARP_MMA) ||
-                      (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H));
+                      (path == VH_PATH_AUTO && R <= kMmaRows && vh::gemv_mma_supported(R, H) &&
+                       (long long)V * H * 2 < kMmaVerifyMaxBytes);
     const bool tensor = !wmma && ((path == VH_PATH_TENSOR) || (path == VH_PATH_AUTO && H % 64 == 0));
     const int mma_group = vh::gemv_mma_supported(kMmaRows, H) ? kMmaRows : 8;  // 16 rows need H <= 5120
     const int group = wmma ? mma_group : tensor ? kTcRows : gemv_group(H);

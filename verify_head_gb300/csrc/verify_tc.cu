@@ -235,6 +235,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
+    // Programmatic dependent launch: the next kernel may start its own prologue now.  The head is
+    // read-only, so the first ring of W stages is requested before this kernel waits for the previous
+    // one; the hidden rows, the draft ids and the workspace are touched only after the wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -242,7 +246,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const unsigned long long pol_w = policy_evict_first();
             const unsigned long long pol_x = policy_evict_last();
             uint32_t it = 0;  // global k-stage counter
-            bool ok = true;
+            bool ok = true, waited = false;
+            // hidden-row loads of the first ring (stage j = it = j, K stage j % k_stages), once the
+            // previous kernel is done
+            auto release_first_ring = [&](uint32_t n) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                for (uint32_t j = 0; j < n; ++j)
+                    tma_load_2d(stage_b + (size_t)j * kStageB, &map_x, &bars->full[j], (int)(j % k_stages) * kBlockK,
+                                0, pol_x);
+                waited = true;
+            };
             for (int tile = blockIdx.x; tile < a.n_tiles && ok; tile += gridDim.x) {
                 for (int ks = 0; ks < k_stages; ++ks, ++it) {
                     const int s = it % kStages;
@@ -251,9 +264,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     mbar_arrive_expect_tx(&bars->full[s], (uint32_t)kStageA + b_bytes);
                     tma_load_2d(stage_a + (size_t)s * kStageA, &map_w, &bars->full[s], ks * kBlockK,
                                 tile * kBlockM, pol_w);
-                    tma_load_2d(stage_b + (size_t)s * kStageB, &map_x, &bars->full[s], ks * kBlockK, 0, pol_x);
+                    if (waited)
+                        tma_load_2d(stage_b + (size_t)s * kStageB, &map_x, &bars->full[s], ks * kBlockK, 0, pol_x);
+                    else if (it + 1 == (uint32_t)kStages)
+                        release_first_ring(it + 1);
                 }
             }
+            if (!waited) release_first_ring(it);  // fewer K stages in all than the ring holds, or a failed wait
             // drain: every issued load must land before the CTA may exit
             const uint32_t issued = it;
             for (uint32_t j = (issued > (uint32_t)kStages ? issued - kStages : 0); j < issued; ++j)
@@ -342,6 +359,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the workspace may come from the previous kernel
     for (int r = threadIdx.x; r < a.R; r += blockDim.x)
         if (merge[r] != 0ull) atomicMax(a.ws.keys + r, merge[r]);
     __threadfence();
@@ -735,8 +753,17 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     auto go = [&](auto kernel, size_t smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kernel<<<grid, kThreadsTc, smem, s>>>(map_w, map_x, a);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreadsTc);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, map_w, map_x, a);
     };
     if (N <= 64) return go(k_verify_tc<8, 64>, smem_bytes_tc(8, 64));
     if (N <= 128) return go(k_verify_tc<6, 128>, smem_bytes_tc(6, 128));
