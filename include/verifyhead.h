@@ -31,11 +31,13 @@
  *  - No global state beyond thread-safe caches of per-device launch facts
  *    (SM count, occupancy): calls are thread-safe given distinct workspaces.
  *  - Kernels launch as programmatic dependents of the previous kernel in the
- *    stream and begin reading their weight table (W_cand, W_full, the 4-bit
- *    tables) before that kernel has finished; everything else is read only
- *    after it has.  Only this library's kernels let a dependent start early,
- *    and none of them writes a weight table, so a table written by any other
- *    operation before the call is always seen complete.
+ *    stream and may begin reading their weight table (W_cand, W_full, the
+ *    4-bit tables) before that kernel has finished; everything else is read
+ *    only after it has.  A kernel lets its dependent start early only if it
+ *    signals so (griddepcontrol.launch_dependents): this library's kernels
+ *    do and never write a weight table.  A table written by a copy, or by a
+ *    kernel that does not signal early, is seen complete; do not write a
+ *    weight table from a kernel that signals early right before a call.
  *  - The same sources also build as libverifyhead_debug.so (-DVH_DEBUG): an
  *    identical ABI whose kernels check their row indices on the device and
  *    report a failed check in the workspace error word (bit 2) instead of
