@@ -685,14 +685,15 @@ def measure_sweep(torch, vh, synth, timer, peaks):
 
 def measure_draft_batch(torch, vh, synth, timer, peaks):
     """The bf16 draft head 65,536 x 2048 for 2 / 4 / 8 / 16 hidden rows per
-    call (warp-level MMAs fed from the weight stream, one pass each): three
-    draft steps per chain as in the bench step, per call = chain / 3."""
+    call (warp-level MMAs fed from the weight stream) and 64 (the tcgen05
+    contraction), one pass each: three draft steps per chain as in the bench
+    step, per call = chain / 3."""
     dev = torch.device("cuda")
-    c = synth.draft_case(Vc=65_536, H=2048, B=16, steps=3, seed=2)
+    c = synth.draft_case(Vc=65_536, H=2048, B=64, steps=3, seed=2)
     Wc = torch.from_numpy(c.W.view(np.int16)).to(dev).view(torch.bfloat16)
     cc = torch.from_numpy(c.cand_ids).to(dev)
     out = {}
-    for B in (2, 4, 8, 16):
+    for B in (2, 4, 8, 16, 64):
         xs = [torch.from_numpy(np.ascontiguousarray(h[:B]).view(np.int16)).to(dev).view(torch.bfloat16)
               for h in c.hidden]
         wsb = vh.workspace(B)
@@ -708,7 +709,8 @@ def measure_draft_batch(torch, vh, synth, timer, peaks):
         nbytes = 65_536 * 2048 * 2 + 65_536 * 4 + B * 2048 * 2
         out[f"B{B}"] = {"timing": "3-call chains, per call", "steps_per_s": round(1e6 / mean, 1), **stats(us),
                         "hbm_frac": round(nbytes / (mean * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                        "kernel": "k_gemv_mma_bf16 (warp MMAs fed from the weight stream)"}
+                        "kernel": ("k_gemv_mma_bf16 (warp MMAs fed from the weight stream)" if B <= 16 else
+                                   "k_verify_tc (tcgen05, one CTA per SM) with candidate-id mapping")}
     del Wc
     return out
 

@@ -93,12 +93,15 @@ VH_API size_t vh_workspace_bytes(int rows);
  *  W_cand    device, bf16 [Vc][H] row-major, 32-byte aligned (a separate copy
  *            of the candidate rows, not a view of the full head)
  *  cand_ids  device, int32 [Vc], ascending and distinct (precondition, not
- *            checked; ties are broken by id either way), values in [0, 2^31)
- *  B         1 <= B <= 256 (processed in groups of 16 hidden rows when H %
- *            256 == 0 and H <= 5120, else of 8; each group reads W_cand
- *            once: 2-16 rows on warp-level MMAs when H % 256 == 0, one row
- *            on the streaming GEMV, or on the warp-level MMAs when H is 256
- *            or 512 or the table is 384 MiB or more)
+ *            checked; up to 16 hidden rows per call, ties are broken by id
+ *            either way, above that by position in cand_ids), values in
+ *            [0, 2^31)
+ *  B         1 <= B <= 256.  B > 16 with H % 64 == 0: all rows in one pass of
+ *            the tcgen05 contraction over W_cand.  Otherwise groups of 16
+ *            hidden rows when H % 256 == 0 and H <= 5120, else of 8, each
+ *            reading W_cand once: 2-16 rows on warp-level MMAs when H % 256
+ *            == 0, one row on the streaming GEMV, or on the warp-level MMAs
+ *            when H is 256 or 512 or the table is 384 MiB or more
  *  H         16 <= H <= 65536, H % 16 == 0
  *  Vc        1 <= Vc <= 2^31 - 1
  *  ids       device, int32 [B] (out)

@@ -8,6 +8,7 @@
 
 #include "../../include/verifyhead.h"
 #include "vh_kernels.h"
+#include "vh_verify.h"
 
 namespace {
 
@@ -69,6 +70,7 @@ int draft_group(int H) { return gemv_mma_supported(16, H) ? 16 : gemv_group(H); 
 
 cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
                                Workspace ws, int32_t* ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    // 17-256 rows (H % 64 == 0): one pass of the tcgen05 contraction over the table.
     // 2-16 rows: the warp MMAs (0.85-0.87 of HBM on 65,536 x 2048 at 2-8 rows), where the GEMV slows with
     // every row it holds.  One row: the CUDA-core GEMV on tables under 384 MiB (it starts faster: 128 MiB 22.6 against
     // 26.3 us, 256 MiB 41.2 against 45.3 us per chained call), the warp MMAs from 384 MiB up (65.2 against
@@ -79,6 +81,7 @@ cudaError_t launch_draft_group(const uint16_t* x, int nb, int H, const uint16_t*
     // 512: 28.4 against 31.6 us; 1,024 x 256: 6.5 against 7.2 us per chained call).
     constexpr long long kOneRowMmaBytes = 384ll << 20;
     const long long bytes = (long long)n_rows * H * 2;
+    if (nb > 16 && H % 64 == 0) return launch_draft_tc(x, nb, H, W, cand, n_rows, ws, ids, maxlogit, s);
     // At H = 512 a one-row draft takes 512-element steps: a row group is then one unit of work, never cut
     // between warps, so a row scores the same bits wherever it sits in the table, as on the GEMV; they are
     // also faster there (131,072 x 512: 28.4 against 28.7 us; 990,000 x 512: 164.6 against 170.0 us).
@@ -131,7 +134,7 @@ vh_status mtp_draft_head_argmax(const void* hidden, const void* W_cand, const in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const vh::Workspace w = make_ws(ws, B);
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
-    const int grp = vh::draft_group(H);
+    const int grp = vh::draft_launch_rows(H, B);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);
         cudaError_t e = vh::launch_draft_group(x + (size_t)b0 * H, nb, H, static_cast<const uint16_t*>(W_cand),

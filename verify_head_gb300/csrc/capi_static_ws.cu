@@ -26,6 +26,7 @@
 
 #include "../../include/verifyhead.h"
 #include "vh_kernels.h"
+#include "vh_verify.h"
 
 namespace {
 
@@ -90,7 +91,7 @@ vh_status mtp_draft_head_argmax_static_ws(const void* hidden, const void* W_cand
         return VH_ERR_LAUNCH;
     }
     const vh::Workspace w = vh::ws_view(scratch);
-    const int grp = vh::draft_group(H);  // the same launch groups and kernels as mtp_draft_head_argmax
+    const int grp = vh::draft_launch_rows(H, B);  // the same launch groups and kernels as mtp_draft_head_argmax
     const uint16_t* x = static_cast<const uint16_t*>(hidden);
     for (int b0 = 0; b0 < B; b0 += grp) {
         const int nb = std::min(grp, B - b0);

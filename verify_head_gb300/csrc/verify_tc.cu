@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "vh_kernels.h"
+#include "vh_verify.h"
 #include "vh_ptx.cuh"
 
 namespace vh {
@@ -77,6 +78,7 @@ struct TcArgs {
     int32_t* next_ids;
     float* maxlogit;
     AcceptTail tail;
+    const int32_t* cand;  // draft head: next_ids[r] = cand[winning row]; nullptr for verify
 };
 
 // ---------------------------------------------------------------------------
@@ -371,7 +373,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
         const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
         vh_guard(k != 0ull, a.err);  // every hidden row has a winner
-        a.next_ids[r] = (int32_t)key_gid(k);
+        const uint32_t gid = key_gid(k);
+        a.next_ids[r] = (int32_t)((a.cand != nullptr && gid < (uint32_t)a.V) ? (uint32_t)__ldg(a.cand + gid) : gid);
         if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
     }
     if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
@@ -628,7 +631,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
         const unsigned long long k = atomicExch(a.ws.keys + r, 0ull);
         vh_guard(k != 0ull, a.err);  // every hidden row has a winner
-        a.next_ids[r] = (int32_t)key_gid(k);
+        const uint32_t gid = key_gid(k);
+        a.next_ids[r] = (int32_t)((a.cand != nullptr && gid < (uint32_t)a.V) ? (uint32_t)__ldg(a.cand + gid) : gid);
         if (a.maxlogit != nullptr) a.maxlogit[r] = key_score(k);
     }
     if (threadIdx.x == 0) atomicExch(a.ws.ticket, 0u);
@@ -680,7 +684,8 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int H, int box_
 
 // CTA-pair launch (R in 129..256): clusters of 2, grid = 2 x the resident clusters.
 static cudaError_t launch_verify_tc2(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
-                                     int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+                                     int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                                     const int32_t* cand) {
     alignas(64) CUtensorMap map_w, map_x;
     if (!make_map(&map_w, W, V, H, kBlockM) || !make_map(&map_x, X, R, H, 128)) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(k_verify_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem2);
@@ -696,6 +701,7 @@ static cudaError_t launch_verify_tc2(const uint16_t* X, int R, int H, const uint
     a.next_ids = next_ids;
     a.maxlogit = maxlogit;
     a.tail = tail;
+    a.cand = cand;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreadsTc);
     cfg.dynamicSmemBytes = kSmem2;
@@ -724,12 +730,13 @@ static cudaError_t launch_verify_tc2(const uint16_t* X, int R, int H, const uint
 }
 }  // namespace tc
 
-cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
-                             int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+static cudaError_t launch_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
+                             int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s,
+                             const int32_t* cand) {
     using namespace tc;
     if (R < 1 || R > kMaxN || H < kBlockK || H % kBlockK != 0 || V < 1) return cudaErrorNotSupported;
     if (R > 128) {
-        cudaError_t e = launch_verify_tc2(X, R, H, W, V, ws, next_ids, maxlogit, tail, s);
+        cudaError_t e = launch_verify_tc2(X, R, H, W, V, ws, next_ids, maxlogit, tail, s, cand);
         if (e != cudaErrorNotSupported) return e;  // otherwise fall through to the single-CTA kernel
     }
     const int N = (R + 15) / 16 * 16;
@@ -746,6 +753,7 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     a.next_ids = next_ids;
     a.maxlogit = maxlogit;
     a.tail = tail;
+    a.cand = cand;
     const int grid = std::max(1, std::min(sm_count(), a.n_tiles));
     // ring depth by width: up to 64 hidden rows take eight stages (20 / 32 / 64 rows on the
     // 248,320 x 2048 head: 157.7-158.1 us against 158.1-160.1 with six and 165.9-167.9 with
@@ -768,6 +776,17 @@ cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W,
     if (N <= 64) return go(k_verify_tc<8, 64>, smem_bytes_tc(8, 64));
     if (N <= 128) return go(k_verify_tc<6, 128>, smem_bytes_tc(6, 128));
     return go(k_verify_tc<4, 256>, smem_bytes_tc(4, 256));
+}
+
+cudaError_t launch_verify_tc(const uint16_t* X, int R, int H, const uint16_t* W, int V, Workspace ws,
+                             int32_t* next_ids, float* maxlogit, const AcceptTail& tail, cudaStream_t s) {
+    return launch_tc(X, R, H, W, V, ws, next_ids, maxlogit, tail, s, nullptr);
+}
+
+cudaError_t launch_draft_tc(const uint16_t* x, int nb, int H, const uint16_t* W, const int32_t* cand, int n_rows,
+                            Workspace ws, int32_t* ids, float* maxlogit, cudaStream_t s) {
+    if (cand == nullptr) return cudaErrorNotSupported;
+    return launch_tc(x, nb, H, W, n_rows, ws, ids, maxlogit, AcceptTail{}, s, cand);
 }
 
 }  // namespace vh
