@@ -20,7 +20,9 @@
  *    check returns a negative status and launches nothing.  VH_ERR_LAUNCH
  *    reports a CUDA launch error (the workspace must then be re-zeroed).
  *  - Argmax rule: the largest fp32 score wins; equal scores go to the lowest
- *    global token id.  NaN scores count as -inf; -0 equals +0.
+ *    global token id (for the draft heads given their precondition of
+ *    ascending candidate ids; see mtp_draft_head_argmax).  NaN scores count
+ *    as -inf; -0 equals +0.
  *  - bf16 tensors are passed as raw 16-bit patterns, row-major.
  *  - Workspace: `ws` is a caller-owned device buffer of at least
  *    vh_workspace_bytes(rows) bytes, 16-byte aligned, zeroed ONCE by the
